@@ -1,0 +1,230 @@
+/* ss.h -- fused LLM sampling and speculative verification on one GB300 GPU.
+ *
+ * C ABI of libss.so.  Every entry point takes plain pointers and sizes; all
+ * tensors are caller-owned device memory unless stated otherwise.  The
+ * library never allocates device memory, never synchronises the device and
+ * never copies to the host inside ss_sample / ss_verify: both are a fixed
+ * sequence of kernel launches on the caller's stream whose launch shapes
+ * depend only on the plan, so a call can be captured in a CUDA Graph and
+ * replayed with new device-resident data (logits, parameters, draft offsets,
+ * seeds).
+ *
+ * What is computed (page titles and sections of the source material):
+ *  - "SonicSampler: unified tile-aware kernels for LLM sampling and
+ *    speculative verification", 3.1 Background: logits processing (grammar
+ *    mask, repetition / frequency / presence penalties, logit bias,
+ *    temperature) is a map over the vocabulary; truncation (top-k, top-p,
+ *    min-p; min-p can be evaluated without a softmax) needs a global
+ *    reduction; sampling is x* = argmax_i (x_i + eps_i) (Gumbel-max, eps = 0
+ *    for greedy); a draft token d is accepted when u q(d) <= p(d), u ~ U(0,1),
+ *    and otherwise a token is resampled from max(0, p - q) normalised.
+ *  - same page, 3.2 Workload-aware execution model and Fig. 1: a two-stage
+ *    hierarchical top-k with k = 128.  Stage 1 runs one program per
+ *    (row, vocabulary tile of B_N tokens) and fuses the prelude with a
+ *    tile-local top-k; only k packed candidates per tile reach HBM.  Stage 2
+ *    runs per row, merges the Z_v * k candidates (Z_v = ceil(V / B_N)) and
+ *    applies truncation, Gumbel noise and argmax.
+ *  - "Decoding and sampling" (dl-note), sections Temperature, Top-k, Top-p,
+ *    Min-p and Combination (Temperature -> Softmax -> top-k/top-p/min-p ->
+ *    Renormalize -> Sample; top-k with top-p keeps the intersection), and
+ *    Rejection Sampler (accept / residual; the output is distributed as p).
+ *
+ * Semantics fixed where the pages are silent:
+ *  - prelude per element, fp32 with one rounding per operation, in this
+ *    order: mask (bit i%32 of word i/32, 1 = allowed, else -inf); if count
+ *    c of token i in the history is > 0 and SS_PENALTY: x = x>0 ? x/rep :
+ *    x*rep, then x -= freq*c, then x -= pres; if SS_BIAS: each bias entry for
+ *    token i is added in list order; stochastic rows: x *= RN(1/T); a NaN
+ *    result becomes -inf (status SS_ST_NAN);
+ *  - candidate order: processed logit descending, token id ascending (-0 and
+ *    +0 are equal); candidates are the first min(128, V) tokens in that order;
+ *  - probabilities are the softmax over those candidates; top-k keeps k,
+ *    top-p keeps token t iff the probability mass before it is < top_p,
+ *    min-p keeps t iff l_t - l_0 >= ln(min_p); the kept set is the shortest
+ *    active prefix and at least one token; greedy rows take the first
+ *    candidate and ignore temperature and truncation;
+ *  - random numbers: Philox-4x32-10 (Salmon et al., SC'11) with key = the
+ *    row's 64-bit seed and counter (i/4, position, row, purpose), word i%4;
+ *    u = ((w >> 9) * 2 + 1) * 2^-24; Gumbel noise -ln(-ln u) in fp32;
+ *    purpose 0 = sample / bonus token (i = token id), 1 = accept uniform
+ *    (i = 0), 2 = residual resampling (i = token id); position =
+ *    rows[r].position + j for draft index j;
+ *  - verification p: the kept distribution for rows that request any
+ *    truncation, else the full-vocabulary softmax; greedy rows accept iff
+ *    the draft equals the argmax.
+ */
+#ifndef SS_H_
+#define SS_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Return codes.  Host-detectable misuse returns a negative code before any
+ * launch; SS_ERR_CUDA means a launch failed (ss_last_error() has the text). */
+typedef enum {
+  SS_OK = 0,
+  SS_ERR_ARG = -1,          /* null pointer, size out of range, B > max_rows */
+  SS_ERR_ALIGN = -2,        /* logits / draft-prob rows not 16-byte aligned */
+  SS_ERR_UNSUPPORTED = -3,  /* vocabulary or tile size outside the plan's range */
+  SS_ERR_WORKSPACE = -4,    /* workspace missing or smaller than ss_workspace_bytes */
+  SS_ERR_CUDA = -5          /* CUDA runtime error */
+} ss_status;
+
+typedef enum { SS_F32 = 0, SS_BF16 = 1 } ss_dtype;
+
+/* Per-row flag bits: the "compact bit-level indicators" that select
+ * per-request behaviour inside one batch (SonicSampler page, section 1). */
+enum {
+  SS_GREEDY = 1u << 0,   /* argmax; ignore temperature and truncation */
+  SS_MASK = 1u << 1,     /* apply the grammar bitmask */
+  SS_PENALTY = 1u << 2,  /* repetition / frequency / presence penalties */
+  SS_BIAS = 1u << 3,     /* sparse logit bias */
+  SS_TOPK = 1u << 4,     /* top_k > 0 keeps the top_k most probable */
+  SS_TOPP = 1u << 5,     /* top_p < 1 keeps the nucleus */
+  SS_MINP = 1u << 6      /* min_p > 0 keeps p >= min_p * p_max */
+};
+
+/* Per-row status bits written to ss_out.row_status.  Data errors never trap. */
+enum {
+  SS_ST_NAN = 1u << 0,         /* a processed logit was NaN; treated as -inf */
+  SS_ST_NO_FINITE = 1u << 1,   /* every candidate is -inf; token = -1 */
+  SS_ST_BAD_HIST = 1u << 2,    /* a history id >= V was ignored */
+  SS_ST_BAD_BIAS = 1u << 3,    /* a bias id >= V was ignored */
+  SS_ST_BAD_PARAM = 1u << 4,   /* invalid parameters: no tokens (-1) */
+  SS_ST_BAD_DRAFT = 1u << 5,   /* a draft id outside [0, V): rejected */
+  SS_ST_POS_INF = 1u << 6,     /* +inf processed logit: point mass on it */
+  SS_ST_RESID_EMPTY = 1u << 7  /* residual max(0, p - q) had no mass: sampled from p */
+};
+
+/* One row's sampling parameters (device array of B entries, 44 bytes each).
+ * Valid ranges: stochastic rows need 0 < temperature < inf; top_p in (0, 1]
+ * when SS_TOPP; min_p in [0, 1] when SS_MINP; top_k >= 0 when SS_TOPK;
+ * rep > 0 and finite freq, pres when SS_PENALTY; 0 <= hist_len <= hist_stride;
+ * 0 <= n_bias <= bias_stride.  A row outside them gets SS_ST_BAD_PARAM. */
+typedef struct {
+  uint32_t flags;
+  float temperature, top_p, min_p;
+  float rep, freq, pres;
+  int32_t top_k;
+  int32_t hist_len;     /* entries of the history row in use; ids < 0 are padding */
+  int32_t n_bias;       /* entries of the bias row in use; ids < 0 are padding */
+  uint32_t position;    /* Philox position of the row's first target position */
+} ss_row_params;
+
+/* One sparse-bias entry (device array [B, bias_stride]). */
+typedef struct {
+  int32_t token;
+  float value;
+} ss_bias_entry;
+
+/* Opaque, immutable plan: vocabulary size, capacities, dtypes and the tile
+ * size B_N, chosen once per shape on the host. */
+typedef struct ss_plan ss_plan;
+
+/* Per-call batch description (host struct; the pointers inside are device
+ * pointers unless noted). */
+typedef struct {
+  int32_t B;                       /* rows in this call, 1 <= B <= max_rows */
+  int64_t ld_logits;               /* row stride of the logits in elements (>= V) */
+  int64_t ld_q;                    /* row stride of draft_probs in elements (>= V) */
+  const ss_row_params* rows;       /* [B] */
+  const int32_t* cu_draft;         /* verify: [B+1] prefix sums of gamma_r, cu_draft[0] = 0 */
+  int32_t hist_stride;             /* ints per history row (>= 1) */
+  int32_t bias_stride;             /* entries per bias row (>= 1) */
+  /* ss_verify only (ss_sample takes these as arguments): */
+  const int32_t* history;          /* [B, hist_stride] or NULL */
+  const uint32_t* bitmask;         /* [B_pos, ceil(V/32)] per target position, or NULL */
+  const ss_bias_entry* bias;       /* [B, bias_stride] or NULL */
+  void* workspace;                 /* caller-allocated device scratch, 256-byte aligned */
+  size_t workspace_bytes;          /* >= ss_workspace_bytes(plan) */
+  void* stream;                    /* cudaStream_t (NULL = legacy default stream) */
+  const ss_plan* plan;
+  void* const* events;             /* optional: 4 cudaEvent_t (timing enabled) recorded on the
+                                      stream before stage 1, after stage 1, after stage 2 and
+                                      after the residual pass (ss_verify) or again after stage 2
+                                      (ss_sample); NULL = none.  Captured into CUDA Graphs as
+                                      event-record nodes. */
+} ss_batch;
+
+/* Outputs (device pointers, caller-owned). */
+typedef struct {
+  int32_t* tokens;         /* sample: [B]; verify: [B, tokens_stride], -1 padded */
+  int32_t tokens_stride;   /* verify: >= max gamma + 1 (ignored by ss_sample) */
+  int32_t* num_accepted;   /* verify: [B] accepted drafts; ignored by ss_sample */
+  int32_t* cand_ids;       /* optional [B_pos, 128]: candidates in order, -1 padded */
+  float* cand_probs;       /* optional [B_pos, 128]: kept renormalised probs, 0 beyond */
+  int32_t* num_kept;       /* optional [B_pos]: kept prefix length */
+  uint32_t* row_status;    /* [B]: SS_ST_* bits */
+} ss_out;
+
+/* Create a plan.  V in [1, 2^20]; max_rows >= 1; max_positions >= max_rows
+ * bounds B_pos (B for sampling, cu_draft[B] + B for verification);
+ * tile = 0 chooses B_N automatically, else 8192 or 16384.  device is the
+ * CUDA ordinal the plan is for.  Returns SS_ERR_ARG / SS_ERR_UNSUPPORTED on
+ * bad sizes; *plan is NULL on failure.  The plan is host memory owned by the
+ * caller (ss_plan_destroy). */
+ss_status ss_plan_create(ss_plan** plan, int32_t V, int32_t max_rows, int32_t max_positions,
+                         ss_dtype logits_dtype, ss_dtype q_dtype, int32_t tile, int32_t device);
+void ss_plan_destroy(ss_plan* plan);
+
+/* Device scratch a call needs: per-tile staging (B_pos * Z_v * 128 entries
+ * of 8 bytes), per-tile metadata and per-row bookkeeping.  Must be zeroed
+ * once before the first call (the library keeps its counters at zero
+ * between calls). */
+size_t ss_workspace_bytes(const ss_plan* plan);
+
+/* Tile size B_N and tile count Z_v the plan uses. */
+int32_t ss_plan_tile(const ss_plan* plan);
+int32_t ss_plan_num_tiles(const ss_plan* plan);
+
+/* Single-step sampling (SonicSampler 3.1-3.2; dl-note Combination).
+ * logits:  [B, ld_logits] fp32 or bf16 (plan dtype), rows 16-byte aligned.
+ * params:  host batch description (B, rows, strides, workspace, stream, plan).
+ * history: [B, hist_stride] int32 or NULL (needed by rows with SS_PENALTY).
+ * bitmask: [B, ceil(V/32)] uint32 or NULL (needed by rows with SS_MASK).
+ * bias:    [B, bias_stride] ss_bias_entry or NULL (needed by rows with SS_BIAS).
+ * seeds:   [B] uint64 Philox keys.
+ * out:     host struct of device outputs: tokens [B], row_status [B], and the
+ *          optional candidate outputs indexed by row.
+ * Asynchronous on params->stream. */
+ss_status ss_sample(const void* logits, const ss_batch* params, const int32_t* history,
+                    const uint32_t* bitmask, const ss_bias_entry* bias, const uint64_t* seeds,
+                    ss_out* out);
+
+/* Speculative verification (SonicSampler 3.1; dl-note Rejection Sampler).
+ * Row r has gamma_r = cu_draft[r+1] - cu_draft[r] drafts and gamma_r + 1
+ * target positions starting at cu_draft[r] + r; gamma_r = 0 is a single-step
+ * row whose bonus token is its sample.
+ * target_logits: [cu_draft[B] + B, ld_logits] (plan dtype).
+ * draft_probs:   [cu_draft[B], ld_q] draft-model probabilities q (plan q dtype).
+ * draft_ids:     [cu_draft[B]] int32.
+ * params:        as for ss_sample, plus cu_draft and the processor inputs
+ *                history / bitmask (per target position) / bias.
+ * seeds:         [B] uint64.
+ * out:           tokens [B, tokens_stride] (accepted drafts, then the
+ *                resampled or bonus token, then -1), num_accepted [B],
+ *                row_status [B], optional candidate outputs per target position.
+ * Asynchronous on params->stream. */
+ss_status ss_verify(const void* target_logits, const void* draft_probs, const int32_t* draft_ids,
+                    const ss_batch* params, const uint64_t* seeds, ss_out* out);
+
+const char* ss_status_str(ss_status s);
+
+/* Text of the last error on the calling host thread ("" if none). */
+const char* ss_last_error(void);
+
+/* Byte offset, inside the workspace, of 8 uint32 diagnostic counters the
+ * kernels increment (0: stage-1 tiles that took the generic radix path,
+ * 1: stage-2 positions that took it, 2: residual passes over V).  They are
+ * cumulative and only cleared by the caller. */
+size_t ss_workspace_diag_offset(const ss_plan* plan);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SS_H_ */

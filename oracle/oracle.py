@@ -56,7 +56,8 @@ class Problem(C.Structure):
                 ("bitmask", C.c_void_p), ("bias_tokens", C.c_void_p),
                 ("bias_values", C.c_void_p), ("bias_stride", C.c_int32),
                 ("seeds", C.c_void_p), ("cu_draft", C.c_void_p), ("draft_ids", C.c_void_p),
-                ("q_bf16", C.c_int32), ("ld_q", C.c_int64), ("draft_probs", C.c_void_p)]
+                ("q_bf16", C.c_int32), ("ld_q", C.c_int64), ("draft_probs", C.c_void_p),
+                ("row_ids", C.c_void_p)]
 
 
 class Outputs(C.Structure):
@@ -127,6 +128,11 @@ def _problem(w, keep: list, rows_override=None):
         P.q_bf16 = 1 if w.q_dtype == "bf16" else 0
         P.ld_q = q.shape[1] if q.ndim == 2 and q.shape[0] else w.V
         P.draft_probs = _ptr(q)
+    rid = getattr(w, "meta", {}).get("row_ids") if hasattr(w, "meta") else None
+    if rid is not None:
+        rid = np.ascontiguousarray(np.asarray(rid, np.int32))
+        keep.append(rid)
+        P.row_ids = _ptr(rid)
     return P
 
 

@@ -106,6 +106,7 @@ struct sso_problem {
   int32_t q_bf16;
   int64_t ld_q;
   const void* draft_probs;    // [cu_draft[B], ld_q]
+  const int32_t* row_ids;     // [B] batch row index used in the Philox counter, or null (= r)
 };
 
 struct sso_outputs {
@@ -424,6 +425,8 @@ void clear_candidates(const sso_outputs& O, int64_t pos) {
 
 // One sampled token from the kept distribution of a position ([DN]
 // Combination; Gumbel-max [SS] 3.1).
+uint32_t philox_row(const sso_problem& P, int r) { return P.row_ids ? (uint32_t)P.row_ids[r] : (uint32_t)r; }
+
 Pick sample_position(const sso_problem& P, int r, uint32_t position, const PosResult& R,
                      uint32_t* status) {
   Pick p;
@@ -433,7 +436,7 @@ Pick sample_position(const sso_problem& P, int r, uint32_t position, const PosRe
   std::vector<int32_t> ids(R.ord.begin(), R.ord.begin() + R.d.n);
   std::vector<float> base(R.d.n);
   for (int t = 0; t < R.d.n; ++t) base[t] = R.x[R.ord[t]];
-  return gumbel_argmax(ids, base, P.seeds[r], position, (uint32_t)r, kPurposeSample);
+  return gumbel_argmax(ids, base, P.seeds[r], position, philox_row(P, r), kPurposeSample);
 }
 
 }  // namespace
@@ -569,7 +572,7 @@ int sso_verify(const sso_problem* Pp, int exact, const sso_outputs* Op) {
       const double pd = p_of(d);
       bool accept = false;
       if (d_ok) {
-        const float u = uniform01(P.seeds[r], 0u, position, (uint32_t)r, kPurposeAccept);
+        const float u = uniform01(P.seeds[r], 0u, position, philox_row(P, r), kPurposeAccept);
         const float prod = u * q_of(d);
         accept = pd > 0.0 && (double)prod <= pd;
         if (O.margin_accept) O.margin_accept[pos] = pd > 0.0 ? std::fabs((double)prod - pd) / pd : kInfD;
@@ -602,10 +605,10 @@ int sso_verify(const sso_problem* Pp, int exact, const sso_outputs* Op) {
         std::vector<float> base2;
         for (size_t t = 0; t < ids.size(); ++t)
           if (resid[t] > 0.0) { ids2.push_back(ids[t]); base2.push_back(logf((float)resid[t])); }
-        pk = gumbel_argmax(ids2, base2, P.seeds[r], position, (uint32_t)r, kPurposeResidual);
+        pk = gumbel_argmax(ids2, base2, P.seeds[r], position, philox_row(P, r), kPurposeResidual);
       } else {
         status |= kStResidEmpty;
-        pk = gumbel_argmax(ids, lbase, P.seeds[r], position, (uint32_t)r, kPurposeResidual);
+        pk = gumbel_argmax(ids, lbase, P.seeds[r], position, philox_row(P, r), kPurposeResidual);
       }
       if (O.margin_resid) O.margin_resid[pos] = pk.margin;
       tok[j] = pk.token;

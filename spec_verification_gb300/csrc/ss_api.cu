@@ -1,0 +1,284 @@
+// Host side of libss.so: plans, argument checks, workspace layout and the
+// fixed launch sequence of ss_sample / ss_verify (see include/ss.h).
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <string>
+
+#include "ss.h"
+#include "ss_common.cuh"
+
+namespace ss {
+const void* stage1_ptr(bool bf16, int BN);
+void stage1_launch(bool bf16, int BN, int grid, size_t smem, cudaStream_t st, const Params& P);
+__global__ void stage2_kernel(const Params P, int verify);
+__global__ void residual_kernel(const Params P);
+size_t stage1_smem_bytes(int BN);
+size_t stage2_smem_bytes(int Z);
+size_t residual_smem_bytes(int BN);
+}  // namespace ss
+
+struct ss_plan {
+  int V, max_rows, max_positions, BN, Z, device, sms;
+  ss_dtype ldt, qdt;
+  int grid1, grid2, grid3;
+  size_t smem1, smem2, smem3;
+  const void* k1;
+  size_t off_staging, off_tmin, off_tlse, off_tst, off_pos, off_rowc, off_rescnt, off_res, off_diag, ws_bytes;
+};
+
+namespace {
+
+thread_local std::string g_err;
+
+ss_status fail(ss_status s, const char* msg) {
+  g_err = msg;
+  return s;
+}
+
+ss_status cuda_fail(cudaError_t e, const char* where) {
+  g_err = std::string(where) + ": " + cudaGetErrorString(e);
+  return SS_ERR_CUDA;
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0u; }
+
+struct DeviceGuard {
+  int prev = -1;
+  explicit DeviceGuard(int dev) {
+    cudaGetDevice(&prev);
+    if (prev != dev) cudaSetDevice(dev);
+  }
+  ~DeviceGuard() {
+    int cur = -1;
+    cudaGetDevice(&cur);
+    if (prev >= 0 && cur != prev) cudaSetDevice(prev);
+  }
+};
+
+}  // namespace
+
+extern "C" {
+
+const char* ss_last_error(void) { return g_err.c_str(); }
+
+const char* ss_status_str(ss_status s) {
+  switch (s) {
+    case SS_OK: return "ok";
+    case SS_ERR_ARG: return "invalid argument";
+    case SS_ERR_ALIGN: return "misaligned row";
+    case SS_ERR_UNSUPPORTED: return "unsupported size";
+    case SS_ERR_WORKSPACE: return "workspace too small";
+    case SS_ERR_CUDA: return "CUDA error";
+  }
+  return "unknown status";
+}
+
+ss_status ss_plan_create(ss_plan** out, int32_t V, int32_t max_rows, int32_t max_positions,
+                         ss_dtype logits_dtype, ss_dtype q_dtype, int32_t tile, int32_t device) {
+  if (out == nullptr) return fail(SS_ERR_ARG, "plan pointer is NULL");
+  *out = nullptr;
+  if (V < 1 || V > (1 << 20)) return fail(SS_ERR_UNSUPPORTED, "V must be in [1, 2^20]");
+  if (max_rows < 1 || max_positions < max_rows || max_positions > (1 << 24))
+    return fail(SS_ERR_ARG, "need 1 <= max_rows <= max_positions <= 2^24");
+  if ((logits_dtype != SS_F32 && logits_dtype != SS_BF16) || (q_dtype != SS_F32 && q_dtype != SS_BF16))
+    return fail(SS_ERR_ARG, "dtype must be SS_F32 or SS_BF16");
+  if (tile != 0 && tile != 8192 && tile != 16384) return fail(SS_ERR_UNSUPPORTED, "tile must be 0, 8192 or 16384");
+  int ndev = 0;
+  cudaError_t e = cudaGetDeviceCount(&ndev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDeviceCount");
+  if (device < 0 || device >= ndev) return fail(SS_ERR_ARG, "device ordinal out of range");
+  DeviceGuard guard(device);
+  int sms = 0;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+  int smem_optin = 0;
+  cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
+
+  const bool bf16 = logits_dtype == SS_BF16;
+  int BN = tile;
+  if (BN == 0) {
+    // Larger tiles halve the staging traffic; keep them only when the work
+    // items still cover several waves of the persistent grid.
+    const long long items16 = (long long)max_positions * ((V + 16383) / 16384);
+    BN = (items16 >= 8LL * sms && V > 16384) ? 16384 : 8192;
+    if ((long long)ss::stage2_smem_bytes((V + BN - 1) / BN) > smem_optin) BN = 16384;
+  }
+  ss_plan* p = new (std::nothrow) ss_plan();
+  if (!p) return fail(SS_ERR_ARG, "out of host memory");
+  p->V = V;
+  p->max_rows = max_rows;
+  p->max_positions = max_positions;
+  p->BN = BN;
+  p->Z = (V + BN - 1) / BN;
+  p->device = device;
+  p->sms = sms;
+  p->ldt = logits_dtype;
+  p->qdt = q_dtype;
+  p->k1 = ss::stage1_ptr(bf16, BN);
+  p->smem1 = ss::stage1_smem_bytes(BN);
+  p->smem2 = ss::stage2_smem_bytes(p->Z);
+  p->smem3 = ss::residual_smem_bytes(BN);
+  if ((long long)p->smem2 > smem_optin || (long long)p->smem1 > smem_optin) {
+    delete p;
+    return fail(SS_ERR_UNSUPPORTED, "vocabulary too large for the stage-2 shared-memory merge");
+  }
+  e = cudaFuncSetAttribute(p->k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p->smem1);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(ss::stage2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p->smem2);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(ss::residual_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p->smem3);
+  int occ1 = 0, occ2 = 0, occ3 = 0;
+  if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ1, p->k1, ss::kNT, p->smem1);
+  if (e == cudaSuccess)
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ2, ss::stage2_kernel, ss::kNT, p->smem2);
+  if (e == cudaSuccess)
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ3, ss::residual_kernel, ss::kNT, p->smem3);
+  if (e != cudaSuccess) {
+    delete p;
+    return cuda_fail(e, "kernel attributes");
+  }
+  const long long items1 = (long long)max_positions * p->Z;
+  p->grid1 = (int)std::min<long long>(items1, (long long)std::max(occ1, 1) * sms);
+  p->grid2 = std::min(max_positions, std::max(occ2, 1) * sms);
+  p->grid3 = (int)std::min<long long>((long long)max_rows * p->Z, (long long)std::max(occ3, 1) * sms);
+
+  // workspace layout (256-byte aligned regions)
+  size_t off = 0;
+  const size_t P = (size_t)max_positions, R = (size_t)max_rows, PZ = P * p->Z;
+  p->off_staging = off; off = align_up(off + PZ * ss::kK * 8, 256);
+  p->off_tmin = off;    off = align_up(off + PZ * 8, 256);
+  p->off_tlse = off;    off = align_up(off + PZ * 8, 256);
+  p->off_tst = off;     off = align_up(off + PZ * 4, 256);
+  p->off_pos = off;     off = align_up(off + P * sizeof(ss::PosResult), 256);
+  p->off_rowc = off;    off = align_up(off + R * 4, 256);
+  p->off_rescnt = off;  off = align_up(off + 4, 256);
+  p->off_res = off;     off = align_up(off + R * sizeof(ss::ResidEntry), 256);
+  p->off_diag = off;    off = align_up(off + 8 * 4, 256);
+  p->ws_bytes = off;
+  *out = p;
+  return SS_OK;
+}
+
+void ss_plan_destroy(ss_plan* plan) { delete plan; }
+
+size_t ss_workspace_bytes(const ss_plan* p) { return p ? p->ws_bytes : 0; }
+int32_t ss_plan_tile(const ss_plan* p) { return p ? p->BN : 0; }
+int32_t ss_plan_num_tiles(const ss_plan* p) { return p ? p->Z : 0; }
+size_t ss_workspace_diag_offset(const ss_plan* p) { return p ? p->off_diag : 0; }
+
+}  // extern "C"
+
+namespace {
+
+ss_status fill_common(const ss_plan* pl, const ss_batch* b, const void* logits, const uint64_t* seeds,
+                      const ss_out* out, ss::Params& P) {
+  if (b->B < 1 || b->B > pl->max_rows) return fail(SS_ERR_ARG, "B must be in [1, max_rows]");
+  if (!logits || !b->rows || !seeds || !out->tokens || !out->row_status)
+    return fail(SS_ERR_ARG, "logits, rows, seeds, tokens and row_status are required");
+  const size_t esz = pl->ldt == SS_BF16 ? 2 : 4;
+  if (b->ld_logits < pl->V) return fail(SS_ERR_ARG, "ld_logits < V");
+  if (!aligned16(logits) || ((size_t)b->ld_logits * esz) % 16 != 0)
+    return fail(SS_ERR_ALIGN, "logit rows must start on 16-byte boundaries");
+  if (b->hist_stride < 1 || b->hist_stride > 16384 || b->bias_stride < 1 || b->bias_stride > 4096)
+    return fail(SS_ERR_ARG, "hist_stride must be in [1, 16384] and bias_stride in [1, 4096]");
+  if (!b->workspace || b->workspace_bytes < pl->ws_bytes)
+    return fail(SS_ERR_WORKSPACE, "workspace missing or smaller than ss_workspace_bytes()");
+  if ((reinterpret_cast<uintptr_t>(b->workspace) & 255u) != 0u)
+    return fail(SS_ERR_ALIGN, "workspace must be 256-byte aligned");
+  std::memset(&P, 0, sizeof(P));
+  P.logits = logits;
+  P.ld = b->ld_logits;
+  P.V = pl->V;
+  P.Z = pl->Z;
+  P.BN = pl->BN;
+  P.logits_bf16 = pl->ldt == SS_BF16;
+  P.rows = b->rows;
+  P.B = b->B;
+  P.hist_stride = b->hist_stride;
+  P.bias_stride = b->bias_stride;
+  P.mask_words = (pl->V + 31) / 32;
+  P.seeds = seeds;
+  P.max_positions = pl->max_positions;
+  char* w = static_cast<char*>(b->workspace);
+  P.ws.staging = reinterpret_cast<unsigned long long*>(w + pl->off_staging);
+  P.ws.tile_min = reinterpret_cast<unsigned long long*>(w + pl->off_tmin);
+  P.ws.tile_lse = reinterpret_cast<float2*>(w + pl->off_tlse);
+  P.ws.tile_status = reinterpret_cast<uint32_t*>(w + pl->off_tst);
+  P.ws.pos = reinterpret_cast<ss::PosResult*>(w + pl->off_pos);
+  P.ws.row_count = reinterpret_cast<uint32_t*>(w + pl->off_rowc);
+  P.ws.resid_count = reinterpret_cast<uint32_t*>(w + pl->off_rescnt);
+  P.ws.resid = reinterpret_cast<ss::ResidEntry*>(w + pl->off_res);
+  P.ws.diag = reinterpret_cast<uint32_t*>(w + pl->off_diag);
+  P.out = *out;
+  return SS_OK;
+}
+
+ss_status launch(const ss_plan* pl, const ss::Params& P, cudaStream_t st, bool verify, void* const* ev) {
+  cudaError_t e = cudaSuccess;
+  auto rec = [&](int i) {
+    if (ev && ev[i] && e == cudaSuccess) e = cudaEventRecord(static_cast<cudaEvent_t>(ev[i]), st);
+  };
+  rec(0);
+  ss::stage1_launch(pl->ldt == SS_BF16, pl->BN, pl->grid1, pl->smem1, st, P);
+  rec(1);
+  ss::stage2_kernel<<<pl->grid2, ss::kNT, pl->smem2, st>>>(P, verify ? 1 : 0);
+  rec(2);
+  if (verify) ss::residual_kernel<<<pl->grid3, ss::kNT, pl->smem3, st>>>(P);
+  rec(3);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+  return SS_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+ss_status ss_sample(const void* logits, const ss_batch* params, const int32_t* history,
+                    const uint32_t* bitmask, const ss_bias_entry* bias, const uint64_t* seeds,
+                    ss_out* out) {
+  if (!params || !out || !params->plan) return fail(SS_ERR_ARG, "params, out and plan are required");
+  const ss_plan* pl = params->plan;
+  if (params->B > pl->max_positions) return fail(SS_ERR_ARG, "B exceeds max_positions");
+  ss::Params P;
+  ss_status s = fill_common(pl, params, logits, seeds, out, P);
+  if (s != SS_OK) return s;
+  P.cu_draft = nullptr;
+  P.history = history;
+  P.bitmask = bitmask;
+  P.bias = bias;
+  DeviceGuard guard(pl->device);
+  return launch(pl, P, static_cast<cudaStream_t>(params->stream), false, params->events);
+}
+
+ss_status ss_verify(const void* target_logits, const void* draft_probs, const int32_t* draft_ids,
+                    const ss_batch* params, const uint64_t* seeds, ss_out* out) {
+  if (!params || !out || !params->plan) return fail(SS_ERR_ARG, "params, out and plan are required");
+  const ss_plan* pl = params->plan;
+  ss::Params P;
+  ss_status s = fill_common(pl, params, target_logits, seeds, out, P);
+  if (s != SS_OK) return s;
+  if (!params->cu_draft || !draft_ids || !draft_probs || !out->num_accepted)
+    return fail(SS_ERR_ARG, "cu_draft, draft_ids, draft_probs and num_accepted are required");
+  if (out->tokens_stride < 1) return fail(SS_ERR_ARG, "tokens_stride must be >= 1");
+  if (params->ld_q < pl->V) return fail(SS_ERR_ARG, "ld_q < V");
+  P.cu_draft = params->cu_draft;
+  P.history = params->history;
+  P.bitmask = params->bitmask;
+  P.bias = params->bias;
+  P.draft_ids = draft_ids;
+  P.q = draft_probs;
+  P.ld_q = params->ld_q;
+  P.q_bf16 = pl->qdt == SS_BF16;
+  DeviceGuard guard(pl->device);
+  return launch(pl, P, static_cast<cudaStream_t>(params->stream), true, params->events);
+}
+
+}  // extern "C"

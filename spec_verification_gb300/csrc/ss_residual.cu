@@ -1,0 +1,209 @@
+// Residual resampling over the whole vocabulary for untruncated stochastic
+// rows (SonicSampler 3.1 "Speculative verification": on rejection sample from
+// p~(x) proportional to max{0, p(x) - q(x)}; dl-note "Rejection Sampler").
+//
+// The row walk of stage 2 queues (row, rejected draft index, target position)
+// entries.  This kernel has a fixed launch shape (persistent CTAs) and loops
+// over (entry, vocabulary tile) items: each tile recomputes the processed
+// logits with the stage-1 prelude, p_i = exp(l_i - LSE) with the LSE stage 2
+// assembled from the tiles' (max, sum exp) partials, r_i = p_i - q_i, and the
+// Gumbel-max score ln r_i + g_i (Philox purpose 2) over r_i > 0.  Tiles combine
+// by a 64-bit atomicMax of (key(score) << 32 | ~token); the last tile of an
+// entry writes the token.  If no r_i is positive, the last tile draws from p
+// itself (Gumbel-max of l_i + g_i over the vocabulary).
+#include "ss_common.cuh"
+
+namespace ss {
+
+namespace {
+
+struct S3Smem {
+  unsigned long long best;
+  int last;
+  int pad;
+};
+
+// Processed logits of 4 consecutive tokens i0..i0+3 of one position (the
+// fp32 steps of the stage-1 prelude); counts come from the tile's aux table.
+__device__ __forceinline__ void prelude4(const Params& P, const RowCtx& rc, int pos, int i0, int n_valid,
+                                         const uint16_t* aux, int t0, const ss_bias_entry* brow,
+                                         bool aux_on, float out[4]) {
+  uint32_t mw = 0xFFFFFFFFu;
+  if ((rc.flags & SS_MASK) && P.bitmask) mw = __ldg(P.bitmask + (size_t)pos * P.mask_words + (i0 >> 5));
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int i = i0 + k;
+    if (k >= n_valid) {
+      out[k] = -INFINITY;
+      continue;
+    }
+    float x = load_scalar(P.logits, P.logits_bf16, (int64_t)pos * P.ld + i);
+    if ((rc.flags & SS_MASK) && P.bitmask && ((mw >> (i & 31)) & 1u) == 0u) x = -INFINITY;
+    if (aux_on) {
+      const uint32_t a = aux[i - t0];
+      if (a != 0u) x = apply_penalty_bias(x, a & 0x7FFFu, (a & 0x8000u) != 0u, i, rc, brow);
+    }
+    if (rc.stoch) x = __fmul_rn(x, rc.rT);
+    if (x != x) x = -INFINITY;
+    out[k] = x;
+  }
+}
+
+// Fill the tile's aux table (history counts incl. drafts before j, bias flags).
+__device__ void build_aux(const Params& P, const RowCtx& rc, int r, int j, int t0, int nt, uint16_t* aux,
+                          bool pen_on, bool bias_on, const ss_bias_entry* brow) {
+  const int tid = threadIdx.x;
+  uint32_t* a32 = reinterpret_cast<uint32_t*>(aux);
+  for (int w = tid; w < (nt + 1) / 2; w += kNT) a32[w] = 0u;
+  __syncthreads();
+  if (pen_on) {
+    const int32_t* hrow = P.history + (size_t)r * P.hist_stride;
+    for (int h = tid; h < rc.hist_len; h += kNT) {
+      const int id = __ldg(hrow + h);
+      if (id >= t0 && id < t0 + nt) atomicAdd(a32 + ((id - t0) >> 1), 1u << (16 * ((id - t0) & 1)));
+    }
+    const int base = __ldg(P.cu_draft + r);
+    const int jn = min(j, __ldg(P.cu_draft + r + 1) - base);
+    for (int s = tid; s < jn; s += kNT) {
+      const int id = __ldg(P.draft_ids + base + s);
+      if (id >= t0 && id < t0 + nt) atomicAdd(a32 + ((id - t0) >> 1), 1u << (16 * ((id - t0) & 1)));
+    }
+  }
+  if (bias_on) {
+    for (int e = tid; e < rc.n_bias; e += kNT) {
+      const int id = brow[e].token;
+      if (id >= t0 && id < t0 + nt) atomicOr(a32 + ((id - t0) >> 1), 0x8000u << (16 * ((id - t0) & 1)));
+    }
+  }
+  __syncthreads();
+}
+
+__device__ __forceinline__ unsigned long long block_max(unsigned long long v, S3Smem& sm) {
+  v = warp_max_u64(v);
+  if ((threadIdx.x & 31) == 0) atomicMax(&sm.best, v);
+  __syncthreads();
+  return sm.best;
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(kNT) residual_kernel(const Params P) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  uint16_t* aux = reinterpret_cast<uint16_t*>(smem_raw);
+  S3Smem& sm = *reinterpret_cast<S3Smem*>(smem_raw + (size_t)P.BN * 2);
+  const int tid = threadIdx.x;
+  const int Z = P.Z, V = P.V;
+  const int count = (int)__ldcg(P.ws.resid_count);
+  const long long total = (long long)count * Z;
+  for (long long item = blockIdx.x; item < total; item += gridDim.x) {
+    const int e = (int)(item / Z);
+    const int tile = (int)(item - (long long)e * Z);
+    ResidEntry* ent = P.ws.resid + e;
+    const int r = __ldcg(&ent->row), j = __ldcg(&ent->j), pos = __ldcg(&ent->pos);
+    const RowCtx rc = make_row(P.rows[r], P.hist_stride, P.bias_stride);
+    const uint32_t position = rc.position + (uint32_t)j;
+    const uint64_t seed = P.seeds[r];
+    const float lse = (float)__ldcg(&P.ws.pos[pos].lse);
+    const int64_t qrow = (int64_t)__ldg(P.cu_draft + r) + j;
+    const bool pen_on = (rc.flags & SS_PENALTY) && P.history != nullptr;
+    const bool bias_on = (rc.flags & SS_BIAS) && P.bias != nullptr;
+    const bool aux_on = pen_on || bias_on;
+    const ss_bias_entry* brow = bias_on ? P.bias + (size_t)r * P.bias_stride : nullptr;
+    const int t0 = tile * P.BN;
+    const int nt = min(P.BN, V - t0);
+    if (tid == 0) {
+      sm.best = 0ull;
+      sm.last = 0;
+    }
+    if (aux_on) build_aux(P, rc, r, j, t0, nt, aux, pen_on, bias_on, brow);
+    else __syncthreads();
+
+    unsigned long long best = 0ull;
+    for (int i0 = t0 + 4 * tid; i0 < t0 + nt; i0 += 4 * kNT) {
+      float x[4];
+      prelude4(P, rc, pos, i0, min(4, t0 + nt - i0), aux, t0, brow, aux_on, x);
+      float rr[4];
+      bool any = false;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        rr[k] = -1.0f;
+        if (x[k] > -INFINITY && i0 + k < t0 + nt) {
+          const float p = expf(x[k] - lse);
+          rr[k] = p - load_scalar(P.q, P.q_bf16, qrow * P.ld_q + i0 + k);
+          any |= rr[k] > 0.0f;
+        }
+      }
+      if (any) {
+        uint32_t c0 = (uint32_t)i0 >> 2, c1 = position, c2 = (uint32_t)r, c3 = 2u;
+        philox10(c0, c1, c2, c3, (uint32_t)seed, (uint32_t)(seed >> 32));
+        const uint32_t wd[4] = {c0, c1, c2, c3};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          if (rr[k] > 0.0f) {
+            const float g = gumbel_of(word_to_uniform(wd[(i0 + k) & 3]));
+            const unsigned long long sc = pack(f2key(__fadd_rn(logf(rr[k]), g)), (uint32_t)(i0 + k));
+            best = sc > best ? sc : best;
+          }
+        }
+      }
+    }
+    best = block_max(best, sm);
+    if (tid == 0) {
+      if (best) atomicMax(&ent->best, best);
+      __threadfence();
+      const uint32_t old = atomicAdd(&ent->arrivals, 1u);
+      sm.last = (old == (uint32_t)(Z - 1)) ? 1 : 0;
+    }
+    __syncthreads();
+    if (sm.last) {
+      __threadfence();
+      const unsigned long long fin = atomicAdd(&ent->best, 0ull);
+      int32_t token;
+      uint32_t extra = 0u;
+      if (fin != 0ull) {
+        token = pk_tok(fin);
+      } else {
+        // no residual mass: Gumbel-max over l_i + g_i, i.e. a draw from p
+        extra = SS_ST_RESID_EMPTY;
+        unsigned long long fb = 0ull;
+        for (int tt = 0; tt < Z; ++tt) {
+          const int u0 = tt * P.BN;
+          const int un = min(P.BN, V - u0);
+          if (aux_on) build_aux(P, rc, r, j, u0, un, aux, pen_on, bias_on, brow);
+          for (int i0 = u0 + 4 * tid; i0 < u0 + un; i0 += 4 * kNT) {
+            float x[4];
+            prelude4(P, rc, pos, i0, min(4, u0 + un - i0), aux, u0, brow, aux_on, x);
+            uint32_t c0 = (uint32_t)i0 >> 2, c1 = position, c2 = (uint32_t)r, c3 = 2u;
+            philox10(c0, c1, c2, c3, (uint32_t)seed, (uint32_t)(seed >> 32));
+            const uint32_t wd[4] = {c0, c1, c2, c3};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              if (x[k] > -INFINITY && i0 + k < u0 + un) {
+                const float g = gumbel_of(word_to_uniform(wd[(i0 + k) & 3]));
+                const unsigned long long sc = pack(f2key(__fadd_rn(x[k], g)), (uint32_t)(i0 + k));
+                fb = sc > fb ? sc : fb;
+              }
+            }
+          }
+          __syncthreads();
+        }
+        if (tid == 0) sm.best = 0ull;
+        __syncthreads();
+        fb = block_max(fb, sm);
+        token = fb ? pk_tok(fb) : -1;
+      }
+      if (tid == 0) {
+        if (j < P.out.tokens_stride) P.out.tokens[(size_t)r * P.out.tokens_stride + j] = token;
+        if (extra) P.out.row_status[r] |= extra;
+        ent->best = 0ull;
+        ent->arrivals = 0u;
+        atomicAdd(P.ws.diag + 2, 1u);
+      }
+    }
+    __syncthreads();
+  }
+}
+
+size_t residual_smem_bytes(int BN) { return (size_t)BN * 2 + sizeof(S3Smem) + 16; }
+
+}  // namespace ss

@@ -1,0 +1,156 @@
+"""Device-resident batch for one ss_sample / ss_verify call.
+
+Uploads a workload (numpy arrays in the input format) into torch CUDA
+tensors laid out as include/ss.h expects, allocates the outputs and the
+workspace once, and issues the call through the ctypes binding.  Torch is
+only used for device memory, host pinned memory and streams.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from . import native
+from .workloads import Workload
+
+
+def pack_rows(rows: dict, B: int) -> np.ndarray:
+    a = np.zeros(B, native.ROW_DTYPE)
+    for f in native.ROW_DTYPE.names:
+        a[f] = rows[f][:B]
+    return a
+
+
+def pack_bias(tokens: np.ndarray, values: np.ndarray) -> np.ndarray:
+    a = np.zeros(tokens.shape, native.BIAS_DTYPE)
+    a["token"] = tokens
+    a["value"] = values
+    return a
+
+
+def _padded_rows(a: np.ndarray, esz: int) -> np.ndarray:
+    """Rows padded to a 16-byte multiple (the ABI's row alignment); padding
+    holds NaN bit patterns, which the kernels must never read as tokens."""
+    if a.ndim != 2:
+        return a
+    per = 16 // esz
+    ld = -(-a.shape[1] // per) * per
+    if ld == a.shape[1]:
+        return a
+    out = np.empty((a.shape[0], ld), a.dtype)
+    out[:, :a.shape[1]] = a
+    out[:, a.shape[1]:] = np.float32(np.nan) if a.dtype == np.float32 else np.uint16(0x7FC0)
+    return out
+
+
+def _as_torch_bits(a: np.ndarray):
+    import torch
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint16:
+        a = a.view(np.int16)
+    elif a.dtype == np.uint32:
+        a = a.view(np.int32)
+    elif a.dtype == np.uint64:
+        a = a.view(np.int64)
+    elif a.dtype.names is not None:
+        a = a.view(np.uint8).reshape(-1)
+    return torch.from_numpy(a)
+
+
+class DeviceRun:
+    """Inputs, outputs and workspace of one call, resident on one GPU."""
+
+    def __init__(self, w: Workload, device: str = "cuda:0", tile: int = 0, max_positions: int | None = None,
+                 candidates: bool = True, tokens_stride: int | None = None, pinned_host: bool = False):
+        import torch
+        self.w = w
+        self.dev = torch.device(device)
+        self.verify = w.is_verify
+        npos = w.n_positions
+        self.plan = native.Plan(w.V, w.B, max_positions or npos, w.dtype,
+                                w.q_dtype if self.verify else "f32", tile, self.dev.index or 0)
+        host = {
+            "logits": _as_torch_bits(_padded_rows(w.logits, 2 if w.dtype == "bf16" else 4)),
+            "rows": _as_torch_bits(pack_rows(w.rows, w.B)),
+            "seeds": _as_torch_bits(w.seeds),
+            "history": _as_torch_bits(w.history.astype(np.int32)),
+            "bias": _as_torch_bits(pack_bias(w.bias_tokens, w.bias_values)),
+        }
+        if w.bitmask is not None:
+            host["bitmask"] = _as_torch_bits(w.bitmask)
+        if self.verify:
+            host["cu_draft"] = _as_torch_bits(w.cu_draft.astype(np.int32))
+            host["draft_ids"] = _as_torch_bits(w.draft_ids.astype(np.int32))
+            host["draft_probs"] = _as_torch_bits(_padded_rows(w.draft_probs, 2 if w.q_dtype == "bf16" else 4))
+        if pinned_host:
+            host = {k: v.pin_memory() for k, v in host.items()}
+        self.host = host
+        self.d = {k: v.to(self.dev) for k, v in host.items()}
+        self.ld_logits = int(self.host["logits"].shape[1])
+        self.ld_q = int(self.host["draft_probs"].shape[1]) if self.verify else 0
+        self.hist_stride = int(w.history.shape[1])
+        self.bias_stride = int(w.bias_tokens.shape[1])
+        i32 = torch.int32
+        if self.verify:
+            ts = tokens_stride if tokens_stride is not None else w.max_gamma + 1
+            self.tokens = torch.full((w.B, ts), -1, dtype=i32, device=self.dev)
+            self.num_accepted = torch.zeros(w.B, dtype=i32, device=self.dev)
+        else:
+            self.tokens = torch.full((w.B,), -1, dtype=i32, device=self.dev)
+            self.num_accepted = None
+        self.row_status = torch.zeros(w.B, dtype=i32, device=self.dev)
+        self.cand_ids = self.cand_probs = self.num_kept = None
+        if candidates:
+            self.cand_ids = torch.full((npos, native.K), -1, dtype=i32, device=self.dev)
+            self.cand_probs = torch.zeros((npos, native.K), dtype=torch.float32, device=self.dev)
+            self.num_kept = torch.zeros(npos, dtype=i32, device=self.dev)
+        self.workspace = torch.zeros(self.plan.workspace_bytes, dtype=torch.uint8, device=self.dev)
+
+    def upload(self, non_blocking: bool = True):
+        """Host -> device copy of every input (pinned host buffers)."""
+        for k, v in self.host.items():
+            self.d[k].copy_(v, non_blocking=non_blocking)
+
+    def input_bytes(self) -> int:
+        return sum(v.numel() * v.element_size() for v in self.host.values())
+
+    def output_bytes(self) -> int:
+        n = self.tokens.numel() * 4 + self.row_status.numel() * 4
+        if self.num_accepted is not None:
+            n += self.num_accepted.numel() * 4
+        return n
+
+    def __call__(self, stream=None, logits=None, draft_probs=None, events=None):
+        d = self.d
+        lg = logits if logits is not None else d["logits"]
+        if self.verify:
+            q = draft_probs if draft_probs is not None else d["draft_probs"]
+            native.ss_verify(self.plan, lg, q, d["draft_ids"], d["rows"], d["cu_draft"], d["seeds"],
+                             workspace=self.workspace, tokens=self.tokens, num_accepted=self.num_accepted,
+                             row_status=self.row_status, history=d["history"], bitmask=d.get("bitmask"),
+                             bias=d["bias"], hist_stride=self.hist_stride, bias_stride=self.bias_stride,
+                             cand_ids=self.cand_ids, cand_probs=self.cand_probs, num_kept=self.num_kept,
+                             B=self.w.B, stream=stream, events=events)
+        else:
+            native.ss_sample(self.plan, lg, d["rows"], d["seeds"], workspace=self.workspace,
+                             tokens=self.tokens, row_status=self.row_status, history=d["history"],
+                             bitmask=d.get("bitmask"), bias=d["bias"], hist_stride=self.hist_stride,
+                             bias_stride=self.bias_stride, cand_ids=self.cand_ids,
+                             cand_probs=self.cand_probs, num_kept=self.num_kept, B=self.w.B, stream=stream,
+                             events=events)
+
+    def results(self) -> dict:
+        import torch
+        torch.cuda.synchronize(self.dev)
+        out = {"tokens": self.tokens.cpu().numpy(),
+               "row_status": self.row_status.cpu().numpy().view(np.uint32)}
+        if self.num_accepted is not None:
+            out["num_accepted"] = self.num_accepted.cpu().numpy()
+        if self.cand_ids is not None:
+            out["cand_ids"] = self.cand_ids.cpu().numpy()
+            out["cand_probs"] = self.cand_probs.cpu().numpy()
+            out["num_kept"] = self.num_kept.cpu().numpy()
+        return out
+
+    def diag(self) -> np.ndarray:
+        o = self.plan.diag_offset
+        return self.workspace[o:o + 32].cpu().numpy().view(np.uint32)

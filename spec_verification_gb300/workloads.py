@@ -427,4 +427,28 @@ def config5(seed: int = 5) -> Workload:
     return mixed_workload(seed, 512, 151936, "f32", name="c5")
 
 
+def subset(w, rows) -> Workload:
+    """The rows `rows` of a workload as a workload of their own.  Their
+    original batch row indices are kept in meta["row_ids"] (random streams
+    are keyed by batch row)."""
+    rows = np.asarray(rows, np.int64)
+    rw = {k: v[rows] for k, v in w.rows.items()}
+    meta = dict(w.meta)
+    meta["row_ids"] = rows.astype(np.int32)
+    if not w.is_verify:
+        return Workload(w.name + "_sub", len(rows), w.V, w.dtype, w.logits[rows], rw, w.history[rows],
+                        None if w.bitmask is None else w.bitmask[rows], w.bias_tokens[rows],
+                        w.bias_values[rows], w.seeds[rows], meta=meta)
+    offs = w.position_offsets()
+    gam = w.gammas()
+    pos = np.concatenate([np.arange(offs[r], offs[r] + gam[r] + 1) for r in rows])
+    qr = np.concatenate([np.arange(w.cu_draft[r], w.cu_draft[r + 1]) for r in rows] + [np.zeros(0, np.int64)])
+    cu = np.zeros(len(rows) + 1, np.int32)
+    cu[1:] = np.cumsum(gam[rows])
+    return Workload(w.name + "_sub", len(rows), w.V, w.dtype, w.logits[pos], rw, w.history[rows],
+                    None if w.bitmask is None else w.bitmask[pos], w.bias_tokens[rows], w.bias_values[rows],
+                    w.seeds[rows], cu_draft=cu, draft_ids=w.draft_ids[qr], draft_probs=w.draft_probs[qr],
+                    q_dtype=w.q_dtype, meta=meta)
+
+
 CONFIGS = {1: config1, 2: config2, 3: config3, 4: config4, 5: config5}

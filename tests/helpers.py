@@ -4,6 +4,7 @@ from __future__ import annotations
 import numpy as np
 
 from spec_verification_gb300 import workloads as W
+from spec_verification_gb300.workloads import subset  # noqa: F401
 
 
 def rows(B: int, **kw) -> dict:
@@ -68,3 +69,21 @@ def chi2_pvalue(counts: np.ndarray, probs: np.ndarray) -> float:
     keep = exp > 0
     # pool tiny expected cells
     return float(stats.chisquare(counts[keep], exp[keep] * counts[keep].sum() / exp[keep].sum()).pvalue)
+
+
+def gpu_rows_as(out: dict, w, rows) -> dict:
+    """GPU outputs of a full batch restricted to `rows` (positions follow)."""
+    rows = np.asarray(rows, np.int64)
+    o = {"tokens": out["tokens"][rows], "row_status": out["row_status"][rows]}
+    if "num_accepted" in out:
+        o["num_accepted"] = out["num_accepted"][rows]
+    if w.is_verify:
+        offs = w.position_offsets()
+        gam = w.gammas()
+        pos = np.concatenate([np.arange(offs[r], offs[r] + gam[r] + 1) for r in rows])
+    else:
+        pos = rows
+    for k in ("cand_ids", "cand_probs", "num_kept"):
+        if k in out:
+            o[k] = out[k][pos]
+    return o

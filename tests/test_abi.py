@@ -1,0 +1,86 @@
+"""CPU-side checks of the C ABI: the library builds, loads and exports every
+function include/ss.h declares; the Python binding's struct layouts match the
+header's field lists; the oracle is never reachable from the product package."""
+import ast
+import ctypes
+import re
+from pathlib import Path
+
+import pytest
+
+ROOT = Path(__file__).resolve().parents[1]
+HEADER = ROOT / "include" / "ss.h"
+
+
+def header_functions():
+    text = HEADER.read_text()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\**\s*(ss_[a-z_]+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from spec_verification_gb300 import build
+    path = build.build()
+    return ctypes.CDLL(str(path))
+
+
+def test_library_exports_every_header_function(lib):
+    names = header_functions()
+    assert {"ss_sample", "ss_verify", "ss_plan_create", "ss_workspace_bytes"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+    from spec_verification_gb300 import native
+    assert set(native.EXPORTS) == set(names)
+
+
+def test_struct_layouts_match_header():
+    from spec_verification_gb300 import native
+    text = re.sub(r"/\*.*?\*/", "", HEADER.read_text(), flags=re.S)
+
+    def fields(struct):
+        body = re.search(r"typedef struct \{([^{}]*)\}\s*" + struct + ";", text, flags=re.S).group(1)
+        out = []
+        for decl in body.split(";"):
+            toks = [t for t in decl.replace("*", " ").replace(",", " ").split() if t != "const"]
+            if not toks:
+                continue
+            out += toks[1:]
+        return out
+
+    assert fields("ss_batch") == [f for f, _ in native.Batch._fields_]
+    assert fields("ss_out") == [f for f, _ in native.Out._fields_]
+    assert fields("ss_row_params") == list(native.ROW_DTYPE.names)
+    assert fields("ss_bias_entry") == list(native.BIAS_DTYPE.names)
+
+
+def test_flag_values_agree():
+    from spec_verification_gb300 import workloads as W
+    text = HEADER.read_text()
+    for name, val in [("SS_GREEDY", W.GREEDY), ("SS_MASK", W.MASK), ("SS_PENALTY", W.PENALTY),
+                      ("SS_BIAS", W.BIAS), ("SS_TOPK", W.TOPK), ("SS_TOPP", W.TOPP), ("SS_MINP", W.MINP)]:
+        m = re.search(name + r" = 1u << (\d+)", text)
+        assert m and (1 << int(m.group(1))) == val, name
+
+
+def test_plan_create_without_gpu_reports_error(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    from spec_verification_gb300 import native
+    with pytest.raises(native.SSError):
+        native.Plan(1000, 4)
+
+
+def test_product_package_never_imports_oracle():
+    pkg = ROOT / "spec_verification_gb300"
+    for f in pkg.rglob("*.py"):
+        tree = ast.parse(f.read_text())
+        for node in ast.walk(tree):
+            if isinstance(node, ast.Import):
+                assert not any(a.name.split(".")[0] == "oracle" for a in node.names), f
+            if isinstance(node, ast.ImportFrom):
+                assert (node.module or "").split(".")[0] != "oracle", f
+    for f in (pkg / "csrc").glob("*"):
+        assert not re.search(r"\bsso_|oracle/|liboracle", f.read_text()), f

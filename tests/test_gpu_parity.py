@@ -1,0 +1,254 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle on seeded
+inputs that span several vocabulary tiles and a ragged last tile, plus the
+edge cases of the method.  Comparison rules: tests/parity.py."""
+import numpy as np
+import pytest
+
+from oracle import oracle as O
+from spec_verification_gb300 import workloads as W
+from tests import parity
+from tests.helpers import gpu_rows_as, sample_case, subset, verify_case
+
+pytestmark = pytest.mark.gpu
+F = W
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _env():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    from spec_verification_gb300 import build
+    build.build()
+    O.build()
+
+
+def run_gpu(w, tile=0, **kw):
+    from spec_verification_gb300.runner import DeviceRun
+    d = DeviceRun(w, tile=tile, **kw)
+    d()
+    return d.results(), d
+
+
+def check(w, tile=0, **kw):
+    gpu, d = run_gpu(w, tile=tile, **kw)
+    if w.is_verify:
+        ora = O.verify(w, tokens_stride=gpu["tokens"].shape[1])
+        rep = parity.compare_verify(w, gpu, ora)
+    else:
+        ora = O.sample(w)
+        rep = parity.compare_sample(w, gpu, ora)
+    assert rep.ok(), rep
+    assert rep.ambiguous <= max(1, rep.checked // 200), rep
+    return gpu, ora, d
+
+
+# ------------------------------------------------------------------ sampling
+
+@pytest.mark.parametrize("tile", [8192, 16384])
+def test_config1_full(tile):
+    check(W.config1(), tile=tile)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("tile", [8192, 16384])
+def test_heterogeneous_sample_ragged(dtype, tile):
+    # V = 40000: 5 tiles of 8192 (last 7232) or 3 of 16384 (last 7232); all processors
+    w = W.sample_workload(21, 16, 40000, dtype)
+    check(w, tile=tile)
+
+
+def test_heterogeneous_sample_no_processors():
+    w = W.sample_workload(22, 16, 50000, "bf16", processors=False)
+    check(w)
+
+
+@pytest.mark.parametrize("tile", [8192, 16384])
+def test_topk_stress_small(tile):
+    check(W.topk_stress_workload(23, 12, 70000), tile=tile)
+
+
+def test_small_vocab_and_tiny_tiles():
+    rng = np.random.default_rng(24)
+    for V in (1, 2, 100, 127, 128, 129, 8192, 8193, 8320):
+        x = (rng.standard_normal((6, V)) * 2).astype(np.float32)
+        flags = np.array([F.GREEDY, 0, F.TOPK | F.TOPP, F.MINP, F.TOPP, F.TOPK], np.uint32)
+        w = sample_case(x, flags=flags, top_k=[0, 0, 7, 0, 0, 3], top_p=[1, 1, 0.8, 1, 0.5, 1],
+                        min_p=[0, 0, 0, 0.1, 0, 0], temperature=[1, 0.7, 1.3, 1, 0.9, 2])
+        check(w)
+
+
+def test_ties_and_constant_rows():
+    V = 20000
+    x = np.zeros((6, V), np.float32)
+    x[1] = np.round(np.random.default_rng(1).standard_normal(V), 0)     # heavy ties
+    x[2, ::3] = 1.0
+    x[3] = -np.inf
+    x[3, 5000] = 2.0
+    x[4] = np.float32(-0.0)
+    x[4, ::2] = 0.0
+    x[5] = np.repeat(np.arange(V // 100, dtype=np.float32), 100)        # sorted runs
+    for fl in (F.GREEDY, F.TOPP):
+        w = sample_case(x, flags=fl, top_p=0.9)
+        check(w)
+
+
+def test_nan_inf_and_masked_rows():
+    rng = np.random.default_rng(2)
+    V = 30000
+    x = rng.standard_normal((7, V)).astype(np.float32)
+    x[0, 17] = np.nan
+    x[1, :] = np.nan                       # every element NaN
+    x[2, 99] = np.inf                      # +inf -> point mass
+    x[3, ::5] = np.nan
+    mask = W.bool_to_mask_bits(rng.random((7, V)) < 0.5)
+    mask[4] = 0                            # all masked
+    mask[5] = 0
+    mask[5, 3] = 1 << 7                    # exactly one allowed token
+    mask[6] = 0
+    mask[6, ::97] = 0xFFFFFFFF             # sparse grammar: a few words allowed
+    for fl in (F.MASK, F.MASK | F.GREEDY, F.MASK | F.TOPP | F.MINP):
+        w = sample_case(x, flags=fl, bitmask=mask, top_p=0.7, min_p=0.05)
+        check(w)
+
+
+def test_bad_params_and_ids():
+    rng = np.random.default_rng(3)
+    V = 9000
+    x = rng.standard_normal((6, V)).astype(np.float32)
+    hist = rng.integers(0, V, (6, 40)).astype(np.int32)
+    hist[1, 3] = V + 5                      # out-of-range history id
+    hist[2, :10] = -1                       # padding
+    btok = rng.integers(0, V, (6, 4)).astype(np.int32)
+    btok[3, 1] = V                          # out-of-range bias id
+    btok[4, 2] = btok[4, 0]                 # duplicate bias id (accumulates)
+    bval = rng.uniform(-3, 3, (6, 4)).astype(np.float32)
+    w = sample_case(x, flags=F.PENALTY | F.BIAS | F.TOPP, history=hist, bias_tokens=btok, bias_values=bval,
+                    top_p=[0.9, 0.9, 0.9, 0.9, 0.9, 1.5], rep=1.2, freq=0.1, pres=0.2,
+                    temperature=[1, 1, 1, 1, 1, 1])
+    w.rows["temperature"][0] = -1.0         # invalid
+    check(w)
+
+
+def test_deterministic_repeat():
+    w = W.sample_workload(25, 8, 60000, "bf16")
+    from spec_verification_gb300.runner import DeviceRun
+    d = DeviceRun(w)
+    d()
+    a = d.results()
+    d()
+    b = d.results()
+    for k in a:
+        assert np.array_equal(a[k], b[k]), k
+
+
+# ------------------------------------------------------------------ verification
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_verify_untruncated(dtype):
+    # config-4 style: no truncation, T = 1, 25% greedy; residual passes over V
+    w = W.verify_workload(31, 12, 30000, np.full(12, 3), dtype, dtype, noise=3.0)
+    gpu, ora, d = check(w)
+    stochastic = (w.rows["flags"] & F.GREEDY) == 0
+    assert np.any(ora["num_accepted"][stochastic] < 3)   # rejections -> residual passes over V
+    assert d.diag()[2] > 0
+
+
+def test_verify_mixed_processors():
+    w = W.mixed_workload(32, 24, 50000, "f32")
+    check(w)
+
+
+@pytest.mark.parametrize("tile", [8192, 16384])
+def test_verify_truncated_bf16(tile):
+    w = W.verify_workload(33, 10, 40000, [1, 2, 3, 4, 0, 5, 6, 7, 2, 1], "bf16", "bf16",
+                          processors=True, truncation=True)
+    check(w, tile=tile)
+
+
+def test_verify_edge_cases():
+    rng = np.random.default_rng(34)
+    V = 9000
+    gam = np.array([2, 2, 1, 0, 3])
+    npos = gam.sum() + len(gam)
+    tgt = rng.standard_normal((npos, V)).astype(np.float32) * 2
+    q = np.abs(rng.standard_normal((gam.sum(), V))).astype(np.float32)
+    q /= q.sum(1, keepdims=True)
+    d = rng.integers(0, V, gam.sum()).astype(np.int32)
+    d[0] = -3                      # out-of-range draft id
+    d[3] = int(np.argmax(tgt[3]))  # row 1, draft 1
+    q[4, :] = 0.0                  # row 2: q(d) = 0 -> accepted when p(d) > 0
+    tgt[5:7, :] = -np.inf          # row 2 positions: no finite logits at all
+    w = verify_case(tgt, q, d, gam, flags=[0, F.GREEDY, F.TOPP, 0, F.TOPK], top_p=0.8, top_k=5)
+    check(w)
+
+
+# ------------------------------------------------------------------ full-size workloads (sampled rows)
+
+def _sampled_full(w, n_rows, seed, tile=0):
+    gpu, d = run_gpu(w, tile=tile)
+    rng = np.random.default_rng(seed)
+    rs = np.sort(rng.choice(w.B, size=min(n_rows, w.B), replace=False))
+    sub = subset(w, rs)
+    g = gpu_rows_as(gpu, w, rs)
+    if w.is_verify:
+        ora = O.verify(sub, tokens_stride=gpu["tokens"].shape[1])
+        rep = parity.compare_verify(sub, g, ora)
+    else:
+        ora = O.sample(sub)
+        rep = parity.compare_sample(sub, g, ora)
+    assert rep.ok(), rep
+    return rep, d
+
+
+def test_config2_full_sampled():
+    _sampled_full(W.config2(), 16, 1)
+
+
+def test_config3_full_sampled():
+    _sampled_full(W.config3(), 12, 2)
+
+
+def test_config4_full_sampled():
+    _sampled_full(W.config4(), 12, 3)
+
+
+def test_config5_full_sampled():
+    _sampled_full(W.config5(), 24, 4)
+
+
+# ------------------------------------------------------------------ graphs
+
+def test_graph_replay_matches_eager():
+    import torch
+    from spec_verification_gb300.runner import DeviceRun
+    w = W.mixed_workload(41, 16, 40000, "f32")
+    d = DeviceRun(w)
+    d()
+    eager = d.results()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        d(stream=s)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        d()
+    d.tokens.fill_(7)
+    g.replay()
+    a = d.results()
+    g.replay()
+    b = d.results()
+    for k in eager:
+        assert np.array_equal(eager[k], a[k]), k
+        assert np.array_equal(a[k], b[k]), k
+    # new device data through the same graph: other seeds -> the oracle's answer for them
+    w2 = W.mixed_workload(41, 16, 40000, "f32")
+    w2.seeds = w2.seeds + np.uint64(12345)
+    d.d["seeds"].copy_(torch.from_numpy(w2.seeds.view(np.int64)))
+    g.replay()
+    got = d.results()
+    ora = O.verify(w2, tokens_stride=got["tokens"].shape[1])
+    rep = parity.compare_verify(w2, got, ora)
+    assert rep.ok(), rep
