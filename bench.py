@@ -1,0 +1,397 @@
+#!/usr/bin/env python3
+"""Throughput of the fused sample / verify call on GB300.
+
+One step = one ss_verify call over the mixed serving batch (B = 512 rows,
+V = 151936 fp32 logits, 60% single-step rows and 40% verify rows with ragged
+gamma in 1..7, every logits processor on): the one workload whose single
+call runs every step of the path (prelude, tile top-128, merge, truncation,
+Gumbel sampling, accept test, residual and bonus tokens).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  `value` is rows per second over all ranks,
+timed with CUDA events around K calls replayed from CUDA graphs with the
+inputs already resident in HBM; `e2e` is the same metric with each step's
+inputs copied from pinned host memory and its tokens copied back inside the
+timed region.  Under torchrun each rank runs its own batch (weak scaling,
+no collective on the data path).  `--impl reference` times the CPU oracle.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "rows/sec and achieved HBM GB/s (% of GB300 peak) per fused sample/verify call"
+FALLBACK_HBM_GBS = 6800.0
+STAGE1_SOURCES = ["spec_verification_gb300/csrc/ss_stage1.cu", "spec_verification_gb300/csrc/ss_common.cuh"]
+
+
+def workload(name: str):
+    from spec_verification_gb300 import workloads as W
+    table = {
+        "c5": (W.config5, "mixed serving batch: B=512, V=151936 fp32, 60% single-step / 40% verify "
+                          "(gamma 1..7), all processors, per-row flags from seed 5"),
+        "c2": (W.config2, "single-step heterogeneous: B=64, V=131072 bf16, all processors"),
+        "c3": (W.config3, "single-step top-k stress: B=256, V=262144 fp32, half near-flat rows"),
+        "c4": (W.config4, "speculative verification: B=32, gamma=4, V=131072 bf16 target and draft probs"),
+        "c1": (W.config1, "single-step: B=4, V=32000 fp32, 2 greedy + 2 stochastic rows"),
+    }
+    fn, desc = table[name]
+    return fn(), desc
+
+
+def read_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def stage1_source_hash() -> str:
+    h = hashlib.sha256()
+    for s in STAGE1_SOURCES:
+        with open(os.path.join(ROOT, s), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(wname: str):
+    """DRAM bytes per stage-1 launch from the committed ncu summary, if it was
+    taken on the current stage-1 source (else None)."""
+    path = os.path.join(ROOT, "profiles", f"stage1_{wname}_ncu.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m = re.search(r"stage1_source_sha256_16:\s*([0-9a-f]+)", text)
+    t = re.search(r"dram_bytes_per_full_launch:\s*([0-9.eE+]+)", text)
+    if not m or not t or m.group(1) != stage1_source_hash():
+        return None
+    return float(t.group(1))
+
+
+class Clocks:
+    """nvidia-smi sampler of SM clocks and throttle reasons."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                                          "-lms", "20", "-i", str(self.index)],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=10)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+_CUDART = None
+
+
+def event_ms(a, b) -> float:
+    """Milliseconds between two timing events recorded by the library (inside
+    a captured graph), read with cudaEventElapsedTime."""
+    global _CUDART
+    import ctypes
+    if _CUDART is None:
+        for name in ("libcudart.so.13", "libcudart.so.12", "libcudart.so"):
+            try:
+                _CUDART = ctypes.CDLL(name)
+                break
+            except OSError:
+                continue
+    f = ctypes.c_float()
+    rc = _CUDART.cudaEventElapsedTime(ctypes.byref(f), ctypes.c_void_p(a.cuda_event), ctypes.c_void_p(b.cuda_event))
+    if rc != 0:
+        raise RuntimeError(f"cudaEventElapsedTime failed ({rc})")
+    return f.value
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def stage1_alg_bytes(w, tile: int) -> int:
+    """Bytes stage 1 must move per launch: each position's logits and (when
+    its row applies the grammar mask) its bitmask row are read once; 128
+    packed 8-byte candidates plus 20 bytes of tile metadata are written per
+    vocabulary tile."""
+    import numpy as np
+    from spec_verification_gb300 import workloads as W
+    z = -(-w.V // tile)
+    s = 2 if w.dtype == "bf16" else 4
+    offs = w.position_offsets()
+    mask_rows = (w.rows["flags"] & W.MASK) != 0
+    per_pos_mask = np.repeat(mask_rows, np.diff(offs)) if w.bitmask is not None else np.zeros(w.n_positions, bool)
+    n = w.n_positions * (w.V * s + z * (128 * 8 + 20))
+    n += int(per_pos_mask.sum()) * 4 * (-(-w.V // 32))
+    return int(n)
+
+
+def cpu_baseline(w, desc_name: str, budget_s: float = 12.0) -> dict:
+    """The oracle, as it stands (bounded k = 128 mode, one thread), on the
+    first rows of the same workload until about budget_s seconds of CPU work."""
+    from oracle import oracle
+    from spec_verification_gb300.workloads import subset
+    oracle.lib()
+    done_rows, npos, t_total = 0, 0, 0.0
+    r = 0
+    while t_total < budget_s and r < w.B:
+        s = subset(w, [r])
+        t0 = time.perf_counter()
+        if s.is_verify:
+            oracle.verify(s)
+        else:
+            oracle.sample(s)
+        t_total += time.perf_counter() - t0
+        done_rows += 1
+        npos += s.n_positions
+        r += 1
+    return {"value": done_rows / t_total, "unit": "rows/s", "cores": 1, "kind": "oracle",
+            "sample": f"first {done_rows} rows ({npos} target positions) of {desc_name}, oracle bounded "
+                      f"k=128 mode, single-threaded, {t_total:.1f} s"}
+
+
+def run_reference(args, w, desc):
+    world, rank, _ = dist_setup()
+    if rank != 0:
+        return
+    from oracle import oracle
+    from spec_verification_gb300.workloads import subset
+    oracle.lib()
+    subs = [subset(w, [r]) for r in range(min(w.B, 64))]
+
+    def step(i):
+        s = subs[i % len(subs)]
+        (oracle.verify if s.is_verify else oracle.sample)(s)
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(args.warmup + i)
+    dt = time.perf_counter() - t0
+    value = args.steps / dt
+    sample = (f"one row (all its target positions) of {args.workload} per step, cycling over the first "
+              f"{len(subs)} rows; oracle bounded k=128 mode, single-threaded")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic", "config": {"workload": desc, "name": args.workload, "B": w.B, "V": w.V},
+            "cpu_baseline": {"kind": "oracle", "cores": 1, "sample": sample, "value": value, "unit": "rows/s"},
+            "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, w, desc):
+    import torch
+    import torch.distributed as dist
+    from spec_verification_gb300 import build
+    from spec_verification_gb300.runner import DeviceRun
+
+    world, rank, local = dist_setup()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    build.build()
+    run = DeviceRun(w, device=str(dev), candidates=False, tile=args.tile)
+    verify = w.is_verify
+    K, Wm = args.steps, args.warmup
+    # two resident copies of the large inputs, alternated between steps
+    lg = [run.d["logits"], run.d["logits"].clone()]
+    qq = [run.d.get("draft_probs"), run.d["draft_probs"].clone() if verify else None]
+    G = max(d for d in range(1, min(10, K) + 1) if K % d == 0)
+    stream = torch.cuda.Stream(device=dev)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(G)]
+    with torch.cuda.stream(stream):
+        for i in range(2):
+            run(logits=lg[i % 2], draft_probs=qq[i % 2])
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for i in range(G):
+            run(logits=lg[i % 2], draft_probs=qq[i % 2], events=ev[i])
+    with torch.cuda.stream(stream):
+        for _ in range(max(1, -(-Wm // G))):
+            graph.replay()
+    stream.synchronize()
+
+    clocks = Clocks(local)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    time.sleep(0.05)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        t_start.record(stream)
+        for _ in range(K // G):
+            graph.replay()
+        t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    ck = clocks.stop()
+    if world > 1:
+        dist.barrier()
+    ms = t_start.elapsed_time(t_end)
+    st1 = [event_ms(ev[i][0], ev[i][1]) for i in range(G)]
+    st2 = [event_ms(ev[i][1], ev[i][2]) for i in range(G)]
+    st3 = [event_ms(ev[i][2], ev[i][3]) for i in range(G)]
+    ms_max = ms
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_max = float(t.item())
+
+    # end to end: inputs from pinned host memory, tokens back, every step
+    e2e = None
+    if not args.no_e2e:
+        hrun = DeviceRun(w, device=str(dev), candidates=False, tile=args.tile, pinned_host=True)
+        E = max(3, min(K, args.e2e_steps))
+        outs = {"tokens": torch.empty(hrun.tokens.shape, dtype=torch.int32, pin_memory=True),
+                "row_status": torch.empty(hrun.row_status.shape, dtype=torch.int32, pin_memory=True)}
+        if verify:
+            outs["num_accepted"] = torch.empty(hrun.num_accepted.shape, dtype=torch.int32, pin_memory=True)
+
+        def e2e_step():
+            hrun.upload(non_blocking=True)
+            hrun()
+            outs["tokens"].copy_(hrun.tokens, non_blocking=True)
+            outs["row_status"].copy_(hrun.row_status, non_blocking=True)
+            if verify:
+                outs["num_accepted"].copy_(hrun.num_accepted, non_blocking=True)
+
+        with torch.cuda.stream(stream):
+            for _ in range(2):
+                e2e_step()
+        stream.synchronize()
+        if world > 1:
+            dist.barrier()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            a.record(stream)
+            for _ in range(E):
+                e2e_step()
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+        ems = a.elapsed_time(b)
+        if world > 1:
+            t = torch.tensor([ems], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ems = float(t.item())
+        e2e = {"value": world * w.B * E / (ems / 1e3), "unit": "rows/s",
+               "h2d_bytes_per_step": hrun.input_bytes(), "d2h_bytes_per_step": hrun.output_bytes(),
+               "steps": E, "ms_per_step": ems / E}
+        del hrun
+
+    peak, peak_kind = read_peaks()
+    tile = run.plan.tile
+    alg1 = stage1_alg_bytes(w, tile)
+    t1 = statistics.mean(st1) / 1e3
+    achieved = alg1 / t1 / 1e9
+    traffic = profiled_traffic(args.workload)
+    counted = w.counted_bytes(tile)
+    value = world * w.B * K / (ms_max / 1e3)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        cpu = cpu_baseline(w, args.workload, args.cpu_seconds)
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world, "steps": K, "warmup": Wm,
+            "ms_per_step": ms_max / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32" if w.dtype == "f32" else "bf16", "data": "synthetic",
+            "config": {"workload": desc, "name": args.workload, "B": w.B, "V": w.V,
+                       "positions": w.n_positions, "tile": tile, "tiles_per_row": run.plan.num_tiles,
+                       "l2": "inputs larger than L2 (two resident copies alternated)",
+                       "graph": f"{G} calls per CUDA graph, {K // G} replays", "parallelism": f"replicas{world}"},
+            "roofline": {"bound": "hbm", "kernel": "stage1", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "peak_kind": peak_kind,
+                         "traffic": traffic, "alg_bytes_per_launch": alg1},
+            "stages_us": {"stage1": 1e3 * statistics.mean(st1), "stage2": 1e3 * statistics.mean(st2),
+                          "residual": 1e3 * statistics.mean(st3) if verify else 0.0},
+            "hbm": {"counted_bytes_per_call": counted, "counted_gbs": counted / (ms_max / K / 1e3) / 1e9,
+                    "counted_frac": counted / (ms_max / K / 1e3) / 1e9 / peak,
+                    "note": "counted = logits + bitmask + draft probs + staging write and read per call"},
+            "clocks": ck,
+            "e2e": e2e,
+            "gpu_launches": K * (3 if verify else 2),
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="c5", choices=["c5", "c2", "c3", "c4", "c1"])
+    ap.add_argument("--tile", type=int, default=0)
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.impl == "ours":
+        args.warmup = max(args.warmup, 3)
+    w, desc = workload(args.workload)
+    if args.impl == "reference":
+        run_reference(args, w, desc)
+    else:
+        run_ours(args, w, desc)
+
+
+if __name__ == "__main__":
+    main()
