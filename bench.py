@@ -135,6 +135,10 @@ _CUDART = None
 def event_ms(a, b) -> float:
     """Milliseconds between two timing events recorded by the library (inside
     a captured graph), read with cudaEventElapsedTime."""
+    try:
+        return a.elapsed_time(b)
+    except (RuntimeError, ValueError):
+        pass
     global _CUDART
     import ctypes
     if _CUDART is None:
@@ -251,6 +255,9 @@ def run_ours(args, w, desc):
     G = max(d for d in range(1, min(10, K) + 1) if K % d == 0)
     stream = torch.cuda.Stream(device=dev)
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(G)]
+    for row in ev:  # torch creates the underlying cudaEvent_t at the first record
+        for e in row:
+            e.record(stream)
     with torch.cuda.stream(stream):
         for i in range(2):
             run(logits=lg[i % 2], draft_probs=qq[i % 2])

@@ -16,7 +16,7 @@ const void* stage1_ptr(bool bf16, int BN);
 void stage1_launch(bool bf16, int BN, int grid, size_t smem, cudaStream_t st, const Params& P);
 __global__ void stage2_kernel(const Params P, int verify);
 __global__ void residual_kernel(const Params P);
-size_t stage1_smem_bytes(int BN);
+size_t stage1_smem_bytes(int BN, bool bf16, int max_rows);
 size_t stage2_smem_bytes(int Z);
 size_t residual_smem_bytes(int BN);
 }  // namespace ss
@@ -27,7 +27,7 @@ struct ss_plan {
   int grid1, grid2, grid3;
   size_t smem1, smem2, smem3;
   const void* k1;
-  size_t off_staging, off_tmin, off_tlse, off_tst, off_pos, off_rowc, off_rescnt, off_res, off_diag, ws_bytes;
+  size_t off_staging, off_tlse, off_tst, off_pos, off_rowc, off_rescnt, off_res, off_diag, ws_bytes;
 };
 
 namespace {
@@ -103,10 +103,10 @@ ss_status ss_plan_create(ss_plan** out, int32_t V, int32_t max_rows, int32_t max
   const bool bf16 = logits_dtype == SS_BF16;
   int BN = tile;
   if (BN == 0) {
-    // Larger tiles halve the staging traffic; keep them only when the work
-    // items still cover several waves of the persistent grid.
-    const long long items16 = (long long)max_positions * ((V + 16383) / 16384);
-    BN = (items16 >= 8LL * sms && V > 16384) ? 16384 : 8192;
+    // 8192-token tiles keep two ring slots per CTA and two CTAs per SM in
+    // shared memory; larger vocabularies switch to 16384 when the stage-2
+    // merge of Z_v * 128 candidates would not fit.
+    BN = 8192;
     if ((long long)ss::stage2_smem_bytes((V + BN - 1) / BN) > smem_optin) BN = 16384;
   }
   ss_plan* p = new (std::nothrow) ss_plan();
@@ -121,7 +121,7 @@ ss_status ss_plan_create(ss_plan** out, int32_t V, int32_t max_rows, int32_t max
   p->ldt = logits_dtype;
   p->qdt = q_dtype;
   p->k1 = ss::stage1_ptr(bf16, BN);
-  p->smem1 = ss::stage1_smem_bytes(BN);
+  p->smem1 = ss::stage1_smem_bytes(BN, bf16, max_rows);
   p->smem2 = ss::stage2_smem_bytes(p->Z);
   p->smem3 = ss::residual_smem_bytes(BN);
   if ((long long)p->smem2 > smem_optin || (long long)p->smem1 > smem_optin) {
@@ -152,7 +152,6 @@ ss_status ss_plan_create(ss_plan** out, int32_t V, int32_t max_rows, int32_t max
   size_t off = 0;
   const size_t P = (size_t)max_positions, R = (size_t)max_rows, PZ = P * p->Z;
   p->off_staging = off; off = align_up(off + PZ * ss::kK * 8, 256);
-  p->off_tmin = off;    off = align_up(off + PZ * 8, 256);
   p->off_tlse = off;    off = align_up(off + PZ * 8, 256);
   p->off_tst = off;     off = align_up(off + PZ * 4, 256);
   p->off_pos = off;     off = align_up(off + P * sizeof(ss::PosResult), 256);
@@ -207,7 +206,6 @@ ss_status fill_common(const ss_plan* pl, const ss_batch* b, const void* logits, 
   P.max_positions = pl->max_positions;
   char* w = static_cast<char*>(b->workspace);
   P.ws.staging = reinterpret_cast<unsigned long long*>(w + pl->off_staging);
-  P.ws.tile_min = reinterpret_cast<unsigned long long*>(w + pl->off_tmin);
   P.ws.tile_lse = reinterpret_cast<float2*>(w + pl->off_tlse);
   P.ws.tile_status = reinterpret_cast<uint32_t*>(w + pl->off_tst);
   P.ws.pos = reinterpret_cast<ss::PosResult*>(w + pl->off_pos);
@@ -221,8 +219,17 @@ ss_status fill_common(const ss_plan* pl, const ss_batch* b, const void* logits, 
 
 ss_status launch(const ss_plan* pl, const ss::Params& P, cudaStream_t st, bool verify, void* const* ev) {
   cudaError_t e = cudaSuccess;
+  // Under stream capture a plain event record is only a fork/join marker;
+  // the external flag makes it an event-record node that fires at replay.
+  unsigned int rec_flags = cudaEventRecordDefault;
+  if (ev) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    e = cudaStreamIsCapturing(st, &cs);
+    if (cs == cudaStreamCaptureStatusActive) rec_flags = cudaEventRecordExternal;
+  }
   auto rec = [&](int i) {
-    if (ev && ev[i] && e == cudaSuccess) e = cudaEventRecord(static_cast<cudaEvent_t>(ev[i]), st);
+    if (ev && ev[i] && e == cudaSuccess)
+      e = cudaEventRecordWithFlags(static_cast<cudaEvent_t>(ev[i]), st, rec_flags);
   };
   rec(0);
   ss::stage1_launch(pl->ldt == SS_BF16, pl->BN, pl->grid1, pl->smem1, st, P);

@@ -36,7 +36,6 @@ struct ResidEntry {
 
 struct Workspace {
   unsigned long long* staging;   // [P * Z * 128] packed candidates
-  unsigned long long* tile_min;  // [P * Z] smallest packed candidate of a full tile, 0 otherwise
   float2* tile_lse;              // [P * Z] (tile max, sum exp(x - max)) when requested
   uint32_t* tile_status;         // [P * Z]
   PosResult* pos;                // [P]
@@ -185,6 +184,20 @@ __device__ __forceinline__ float apply_penalty_bias(float x, uint32_t c, bool ha
   return x;
 }
 
+// Out-of-line form for the unrolled hot loops: only the few tokens that are
+// in the history or the bias list take it, and keeping it out of line keeps
+// those loops small enough for the instruction cache.
+static __device__ __noinline__ float penalize_token(float x, uint32_t a, int tok, uint32_t flags, float rep, float freq,
+                                             float pres, int n_bias, const ss_bias_entry* brow) {
+  RowCtx rc;
+  rc.flags = flags;
+  rc.rep = rep;
+  rc.freq = freq;
+  rc.pres = pres;
+  rc.n_bias = n_bias;
+  return apply_penalty_bias(x, a & 0x7FFFu, (a & 0x8000u) != 0u, tok, rc, brow);
+}
+
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
@@ -271,31 +284,75 @@ __device__ __forceinline__ unsigned long long warp_min_u64(unsigned long long v)
   return v;
 }
 
+// Block-wide max / min of a 64-bit value through per-warp slots (no 64-bit
+// shared-memory atomics, which serialise under contention).  All threads
+// call; `slots` holds kNT/32 values; every thread gets the result.
+__device__ __forceinline__ unsigned long long block_max_u64(unsigned long long v, unsigned long long* slots) {
+  v = warp_max_u64(v);
+  if ((threadIdx.x & 31) == 0) slots[threadIdx.x >> 5] = v;
+  __syncthreads();
+  unsigned long long r = slots[0];
+#pragma unroll
+  for (int w = 1; w < kNT / 32; ++w) r = slots[w] > r ? slots[w] : r;
+  __syncthreads();
+  return r;
+}
+__device__ __forceinline__ unsigned long long block_min_u64(unsigned long long v, unsigned long long* slots) {
+  v = warp_min_u64(v);
+  if ((threadIdx.x & 31) == 0) slots[threadIdx.x >> 5] = v;
+  __syncthreads();
+  unsigned long long r = slots[0];
+#pragma unroll
+  for (int w = 1; w < kNT / 32; ++w) r = slots[w] < r ? slots[w] : r;
+  __syncthreads();
+  return r;
+}
+
 // Shared-memory state of the histogram select.
 struct SelectSmem {
   uint32_t hist[256];
   int scan[kNT / 32];
-  int bstar, above, tcnt, pad;
+  int bstar, above, nb, pad;
+  int tcnt[2];
 };
 
 // Find the histogram bin b* holding the need-th largest element:
 // above(b*) < need <= above(b*) + hist[b*], above(b) = sum of bins > b.
-// All threads call; the result is in S.bstar / S.above after the call.
+// Warp 0 scans the 256 bins (8 per lane, from the top); all threads call and
+// read S.bstar / S.above after the call.
 __device__ __forceinline__ void boundary_bin(SelectSmem& S, int need) {
   const int t = threadIdx.x;
-  if (t == 0) {
-    S.bstar = 0;
-    S.above = 0;
-  }
-  const int b = 255 - t;
-  const int v = (t < 256) ? (int)S.hist[b] : 0;
-  int total;
-  const int incl = block_inclusive_scan(v, S.scan, &total);
-  if (t < 256) {
-    const int above = incl - v;
+  if (t < 32) {
+    int v[8];
+    int sum = 0;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      v[q] = (int)S.hist[255 - (t * 8 + q)];  // lane t holds bins 255-8t .. 248-8t
+      sum += v[q];
+    }
+    int incl = sum;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, incl, d);
+      if (t >= d) incl += o;
+    }
+    int above = incl - sum;  // count in bins above this lane's first bin
+    if (t == 0) {
+      S.bstar = 0;
+      S.above = 0;
+      S.nb = 0;
+    }
+    __syncwarp();
     if (above < need && need <= incl) {
-      S.bstar = b;
-      S.above = above;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        if (above < need && need <= above + v[q]) {
+          S.bstar = 255 - (t * 8 + q);
+          S.above = above;
+          S.nb = v[q];
+        }
+        above += v[q];
+      }
     }
   }
   __syncthreads();
@@ -317,6 +374,12 @@ template <class Emit>
 __device__ void block_select(unsigned long long* cand, unsigned long long* tmp, int n, int need,
                              unsigned long long lo, unsigned long long hi, SelectSmem& S, Emit emit) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid < 256) S.hist[tid] = 0u;
+  if (tid == 0) {
+    S.tcnt[0] = 0;
+    S.tcnt[1] = 0;
+  }
+  __syncthreads();
   for (int iter = 0; iter < 16; ++iter) {
     if (need <= 0) break;
     if (n <= need) {
@@ -325,9 +388,10 @@ __device__ void block_select(unsigned long long* cand, unsigned long long* tmp, 
     }
     if (n <= 32) {
       if (warp == 0) {
-        const unsigned long long c = lane < n ? cand[lane] : 0ull;
+        const unsigned long long c = lane < n ? cand[lane] : 0ull;  // empty lanes rank last
         int rank = 0;
-        for (int k = 0; k < n; ++k) {
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
           const unsigned long long o = __shfl_sync(0xffffffffu, c, k);
           rank += (o > c) ? 1 : 0;
         }
@@ -338,25 +402,26 @@ __device__ void block_select(unsigned long long* cand, unsigned long long* tmp, 
     const unsigned long long span = hi - lo;
     int shift = 0;
     if (span != 0ull) shift = max(0, 64 - __clzll((long long)span) - 8);
-    if (tid < 256) S.hist[tid] = 0u;
-    if (tid == 0) S.tcnt = 0;
-    __syncthreads();
     for (int i = tid; i < n; i += kNT) atomicAdd(&S.hist[bin_of(cand[i], lo, shift)], 1u);
     __syncthreads();
     boundary_bin(S, need);
     const uint32_t bs = (uint32_t)min(max(S.bstar, 0), 255);
     const int ab = S.above;
-    const int nb = (int)S.hist[bs];
+    const int nb = S.nb;
+    int* tc = &S.tcnt[iter & 1];
     for (int i = tid; i < n; i += kNT) {
       const unsigned long long c = cand[i];
       const uint32_t b = bin_of(c, lo, shift);
       if (b > bs) {
         emit(c);
       } else if (b == bs) {
-        const int s = atomicAdd(&S.tcnt, 1);
+        const int s = atomicAdd(tc, 1);
         if (s < n) tmp[s] = c;
       }
     }
+    // ready for the next round: histogram cleared, the other counter reset
+    if (tid < 256) S.hist[tid] = 0u;
+    if (tid == 0) S.tcnt[(iter + 1) & 1] = 0;
     __syncthreads();
     need -= ab;
     n = nb;

@@ -18,7 +18,7 @@ namespace ss {
 namespace {
 
 struct S3Smem {
-  unsigned long long best;
+  unsigned long long slots[kNT / 32];
   int last;
   int pad;
 };
@@ -78,13 +78,6 @@ __device__ void build_aux(const Params& P, const RowCtx& rc, int r, int j, int t
   __syncthreads();
 }
 
-__device__ __forceinline__ unsigned long long block_max(unsigned long long v, S3Smem& sm) {
-  v = warp_max_u64(v);
-  if ((threadIdx.x & 31) == 0) atomicMax(&sm.best, v);
-  __syncthreads();
-  return sm.best;
-}
-
 }  // namespace
 
 __global__ void __launch_bounds__(kNT) residual_kernel(const Params P) {
@@ -111,10 +104,7 @@ __global__ void __launch_bounds__(kNT) residual_kernel(const Params P) {
     const ss_bias_entry* brow = bias_on ? P.bias + (size_t)r * P.bias_stride : nullptr;
     const int t0 = tile * P.BN;
     const int nt = min(P.BN, V - t0);
-    if (tid == 0) {
-      sm.best = 0ull;
-      sm.last = 0;
-    }
+    if (tid == 0) sm.last = 0;
     if (aux_on) build_aux(P, rc, r, j, t0, nt, aux, pen_on, bias_on, brow);
     else __syncthreads();
 
@@ -147,7 +137,7 @@ __global__ void __launch_bounds__(kNT) residual_kernel(const Params P) {
         }
       }
     }
-    best = block_max(best, sm);
+    best = block_max_u64(best, sm.slots);
     if (tid == 0) {
       if (best) atomicMax(&ent->best, best);
       __threadfence();
@@ -187,9 +177,7 @@ __global__ void __launch_bounds__(kNT) residual_kernel(const Params P) {
           }
           __syncthreads();
         }
-        if (tid == 0) sm.best = 0ull;
-        __syncthreads();
-        fb = block_max(fb, sm);
+        fb = block_max_u64(fb, sm.slots);
         token = fb ? pk_tok(fb) : -1;
       }
       if (tid == 0) {

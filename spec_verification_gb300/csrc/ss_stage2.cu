@@ -26,22 +26,13 @@ namespace {
 struct S2Smem {
   SelectSmem sel;
   unsigned long long top[kK];
-  unsigned long long lo, hi, tau2, best;
+  unsigned long long slots[kNT / 32];
   int r, j, gamma, cnt, out_cnt, last;
   uint32_t status;
   int d_found;
   float d_l;
   double pd, lse, red[kNT / 32];
 };
-
-__device__ __forceinline__ unsigned long long block_max_u64(unsigned long long v, S2Smem& sm) {
-  v = warp_max_u64(v);
-  if ((threadIdx.x & 31) == 0) atomicMax(&sm.best, v);
-  __syncthreads();
-  const unsigned long long r = sm.best;
-  __syncthreads();
-  return r;
-}
 
 // Exclusive prefix sum of v over threads 0..kNT-1 in fp64.
 __device__ __forceinline__ double block_exclusive_scan_d(double v, double* scratch) {
@@ -126,10 +117,6 @@ __global__ void __launch_bounds__(kNT) stage2_kernel(const Params P, int verify)
       sm.gamma = g;
       sm.cnt = 0;
       sm.out_cnt = 0;
-      sm.lo = ~0ull;
-      sm.hi = 0ull;
-      sm.tau2 = 0ull;
-      sm.best = 0ull;
       sm.status = 0u;
       sm.d_found = 0;
       sm.pd = 0.0;
@@ -169,44 +156,48 @@ __global__ void __launch_bounds__(kNT) stage2_kernel(const Params P, int verify)
           if (P.bias[(size_t)r * P.bias_stride + e].token >= V) atomicOr(&sm.status, (uint32_t)SS_ST_BAD_BIAS);
       }
       // ---- 1. merge the tiles' candidates
+      // Load the Z_v * 128 packed candidates; a tile whose 128 slots are all
+      // real certifies 128 candidates >= its smallest one, so tau2 = the
+      // largest such minimum bounds the position's top-128 from below.
       const size_t tbase = (size_t)pos * Z;
-      unsigned long long tm = 0ull;
       uint32_t tst = 0u;
-      for (int t = tid; t < Z; t += kNT) {
-        const unsigned long long v = P.ws.tile_min[tbase + t];
-        tm = v > tm ? v : tm;
-        tst |= P.ws.tile_status[tbase + t];
-      }
-      tm = warp_max_u64(tm);
-      if (lane == 0 && tm) atomicMax(&sm.tau2, tm);
+      for (int t = tid; t < Z; t += kNT) tst |= P.ws.tile_status[tbase + t];
       if (tst) atomicOr(&sm.status, tst);
-      __syncthreads();
-      const unsigned long long tau2 = sm.tau2;
       const unsigned long long* stg = P.ws.staging + tbase * kK;
+      for (int i = tid; i < cap; i += kNT) tmp[i] = stg[i];
+      __syncthreads();
+      unsigned long long tm = 0ull;
+      for (int t = tid >> 5; t < Z; t += kNT / 32) {
+        unsigned long long mn = ~0ull;
+#pragma unroll
+        for (int q = 0; q < kK / 32; ++q) {
+          const unsigned long long c = tmp[t * kK + q * 32 + lane];
+          mn = c < mn ? c : mn;   // an empty slot (0) makes the tile certify nothing
+        }
+        mn = warp_min_u64(mn);
+        tm = mn > tm ? mn : tm;
+      }
+      const unsigned long long tau2 = block_max_u64(tm, sm.slots);
       unsigned long long lmin = ~0ull, lmax = 0ull;
       for (int i = tid; i < cap; i += kNT) {
-        const unsigned long long c = stg[i];
+        const unsigned long long c = tmp[i];
         if (c != 0ull && c >= tau2) {
           cand[atomicAdd(&sm.cnt, 1)] = c;
           lmin = c < lmin ? c : lmin;
           lmax = c > lmax ? c : lmax;
         }
       }
-      lmin = warp_min_u64(lmin);
-      lmax = warp_max_u64(lmax);
-      if (lane == 0) {
-        atomicMin(&sm.lo, lmin);
-        atomicMax(&sm.hi, lmax);
-      }
-      __syncthreads();
+      const unsigned long long lo = block_min_u64(lmin, sm.slots);
+      const unsigned long long hi = block_max_u64(lmax, sm.slots);
       const int n = sm.cnt;
       const int need = min(kK, V);
-      block_select(cand, tmp, n, need, sm.lo, sm.hi, sm.sel,
+      block_select(cand, tmp, n, need, lo, hi, sm.sel,
                    [&](unsigned long long c) {
                      const int s = atomicAdd(&sm.out_cnt, 1);
                      if (s < kK) sm.top[s] = c;
                    });
-      if (tid < kK && tid >= need) sm.top[tid] = 0ull;
+      // slots the select did not fill (only if its count invariant broke) stay empty
+      if (tid < kK && tid >= min(sm.out_cnt, need)) sm.top[tid] = 0ull;
       __syncthreads();
       // bitonic sort of the 128 candidates, descending
       for (int k = 2; k <= kK; k <<= 1) {
@@ -291,7 +282,7 @@ __global__ void __launch_bounds__(kNT) stage2_kernel(const Params P, int verify)
             const float g = gumbel_of(philox_uniform(seed, (uint32_t)tok, position, (uint32_t)r, 0u));
             sc = pack(f2key(__fadd_rn(l, g)), (uint32_t)tok);
           }
-          token = pk_tok(block_max_u64(sc, sm));
+          token = pk_tok(block_max_u64(sc, sm.slots));
         }
       } else {
         // ---- 4. verification of draft j
@@ -353,7 +344,7 @@ __global__ void __launch_bounds__(kNT) stage2_kernel(const Params P, int verify)
                   sc = pack(f2key(__fadd_rn(l, g)), (uint32_t)tok);
                 }
               }
-              token = pk_tok(block_max_u64(sc, sm));
+              token = pk_tok(block_max_u64(sc, sm.slots));
               if (!anypos && tid == 0) atomicOr(&sm.status, (uint32_t)SS_ST_RESID_EMPTY);
             } else {
               token = kPending;  // drawn by the pass over the vocabulary

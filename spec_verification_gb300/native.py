@@ -139,6 +139,7 @@ def _events(events):
     if events is None:
         return None
     assert len(events) == 4
+    assert all(e.cuda_event for e in events), "record each event once first (torch creates them lazily)"
     return (C.c_void_p * 4)(*[e.cuda_event for e in events])
 
 
