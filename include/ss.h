@@ -212,6 +212,33 @@ ss_status ss_sample(const void* logits, const ss_batch* params, const int32_t* h
 ss_status ss_verify(const void* target_logits, const void* draft_probs, const int32_t* draft_ids,
                     const ss_batch* params, const uint64_t* seeds, ss_out* out);
 
+/* ss_sample_noalloc -- the source material has no counterpart to this call;
+ * it is an addition of this library.  It is ss_sample for callers that cannot
+ * provide the workspace: a runtime that hands nearly all free device memory
+ * to its own pool (a KV cache) and exposes no allocator, or a C caller in a
+ * decode loop that must not call cudaMalloc / cudaFree because both
+ * synchronise the device.  It allocates nothing.
+ *
+ * Arguments, outputs and results are those of ss_sample; params->workspace
+ * and params->workspace_bytes are ignored.  The scratch is a device array
+ * of SS_NOALLOC_SCRATCH_BYTES inside libss.so, one per device per process:
+ *  - the first call for a device (the plan's device) does the set-up: it
+ *    looks the array's address up and clears it on params->stream.  Make
+ *    that first call before any stream capture; under capture it returns
+ *    SS_ERR_ARG;
+ *  - the whole array starts at zero (set-up clears it); the counters in it
+ *    must be zero when a call starts, and each completed call leaves them
+ *    at zero again;
+ *  - plans whose ss_workspace_bytes exceeds SS_NOALLOC_SCRATCH_BYTES are
+ *    rejected with SS_ERR_UNSUPPORTED (use ss_sample with a workspace);
+ *  - calls on the same device that overlap in time (different streams or
+ *    host threads without ordering between them) share the array and race:
+ *    order them on one stream or serialise them. */
+#define SS_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20) /* 16 MiB */
+ss_status ss_sample_noalloc(const void* logits, const ss_batch* params, const int32_t* history,
+                            const uint32_t* bitmask, const ss_bias_entry* bias, const uint64_t* seeds,
+                            ss_out* out);
+
 const char* ss_status_str(ss_status s);
 
 /* Text of the last error on the calling host thread ("" if none). */

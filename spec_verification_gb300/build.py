@@ -17,7 +17,7 @@ CSRC = PKG / "csrc"
 INCLUDE = ROOT / "include"
 BUILD = PKG / "_build"
 LIB = BUILD / "libss.so"
-SOURCES = ["ss_api.cu", "ss_stage1.cu", "ss_stage2.cu", "ss_residual.cu"]
+SOURCES = ["ss_api.cu", "ss_stage1.cu", "ss_stage2.cu", "ss_residual.cu", "ss_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

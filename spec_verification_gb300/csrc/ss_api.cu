@@ -289,3 +289,9 @@ ss_status ss_verify(const void* target_logits, const void* draft_probs, const in
 }
 
 }  // extern "C"
+
+namespace ss {
+// Used by the static-scratch entry point (ss_noalloc.cu).
+int plan_device(const ss_plan* p) { return p->device; }
+void set_last_error(const char* msg) { g_err = msg; }
+}  // namespace ss

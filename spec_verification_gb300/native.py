@@ -48,7 +48,7 @@ class Out(C.Structure):
 
 EXPORTS = ["ss_plan_create", "ss_plan_destroy", "ss_workspace_bytes", "ss_plan_tile",
            "ss_plan_num_tiles", "ss_sample", "ss_verify", "ss_status_str", "ss_last_error",
-           "ss_workspace_diag_offset"]
+           "ss_workspace_diag_offset", "ss_sample_noalloc"]
 
 _lib = None
 
@@ -77,6 +77,8 @@ def library() -> C.CDLL:
     L.ss_sample.argtypes = [C.c_void_p, C.POINTER(Batch), C.c_void_p, C.c_void_p, C.c_void_p,
                             C.c_void_p, C.POINTER(Out)]
     L.ss_sample.restype = C.c_int
+    L.ss_sample_noalloc.argtypes = L.ss_sample.argtypes
+    L.ss_sample_noalloc.restype = C.c_int
     L.ss_verify.argtypes = [C.c_void_p, C.c_void_p, C.c_void_p, C.POINTER(Batch), C.c_void_p,
                             C.POINTER(Out)]
     L.ss_verify.restype = C.c_int
@@ -164,6 +166,29 @@ def ss_sample(plan: Plan, logits, rows, seeds, *, workspace, tokens, row_status,
     o.cand_ids, o.cand_probs, o.num_kept = _ptr(cand_ids), _ptr(cand_probs), _ptr(num_kept)
     _check(library().ss_sample(_ptr(logits), C.byref(b), _ptr(history), _ptr(bitmask), _ptr(bias),
                                _ptr(seeds), C.byref(o)))
+
+
+def ss_sample_noalloc(plan: Plan, logits, rows, seeds, *, tokens, row_status, history=None,
+                      bitmask=None, bias=None, hist_stride=1, bias_stride=1, cand_ids=None,
+                      cand_probs=None, num_kept=None, B=None, stream=None, events=None):
+    """ss_sample_noalloc: ss_sample with the library's static device scratch
+    (no workspace argument)."""
+    b = Batch()
+    b.B = B if B is not None else seeds.shape[0]
+    b.ld_logits = logits.stride(0)
+    b.ld_q = 0
+    b.rows = _ptr(rows)
+    b.hist_stride, b.bias_stride = hist_stride, bias_stride
+    b.workspace, b.workspace_bytes = None, 0
+    b.stream = _stream_ptr(stream)
+    b.plan = plan.handle
+    ev = _events(events)
+    b.events = C.cast(ev, C.c_void_p) if ev is not None else None
+    o = Out()
+    o.tokens, o.tokens_stride, o.row_status = _ptr(tokens), 1, _ptr(row_status)
+    o.cand_ids, o.cand_probs, o.num_kept = _ptr(cand_ids), _ptr(cand_probs), _ptr(num_kept)
+    _check(library().ss_sample_noalloc(_ptr(logits), C.byref(b), _ptr(history), _ptr(bitmask),
+                                       _ptr(bias), _ptr(seeds), C.byref(o)))
 
 
 def ss_verify(plan: Plan, target_logits, draft_probs, draft_ids, rows, cu_draft, seeds, *, workspace,
