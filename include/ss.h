@@ -181,6 +181,11 @@ size_t ss_workspace_bytes(const ss_plan* plan);
 int32_t ss_plan_tile(const ss_plan* plan);
 int32_t ss_plan_num_tiles(const ss_plan* plan);
 
+/* CTAs of the stage-1 launch.  Stage 1 splits the B_pos * Z_v tiles into
+ * min(this, B_pos * Z_v) contiguous runs, one per CTA; a run's part inside
+ * one position is a segment, which leaves one list of 128 candidates. */
+int32_t ss_plan_stage1_ctas(const ss_plan* plan);
+
 /* Single-step sampling (SonicSampler 3.1-3.2; dl-note Combination).
  * logits:  [B, ld_logits] fp32 or bf16 (plan dtype), rows 16-byte aligned.
  * params:  host batch description (B, rows, strides, workspace, stream, plan).

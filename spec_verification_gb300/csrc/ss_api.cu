@@ -12,17 +12,18 @@
 #include "ss_common.cuh"
 
 namespace ss {
-const void* stage1_ptr(bool bf16, int BN);
-void stage1_launch(bool bf16, int BN, int grid, size_t smem, cudaStream_t st, const Params& P);
+const void* stage1_ptr(bool bf16);
+void stage1_launch(bool bf16, int grid, size_t smem, cudaStream_t st, const Params& P);
 __global__ void stage2_kernel(const Params P, int verify);
 __global__ void residual_kernel(const Params P);
-size_t stage1_smem_bytes(int BN, bool bf16, int max_rows);
+size_t stage1_smem_bytes(int BN, bool bf16, int nslot);
+int stage1_max_slots();
 size_t stage2_smem_bytes(int Z);
 size_t residual_smem_bytes(int BN);
 }  // namespace ss
 
 struct ss_plan {
-  int V, max_rows, max_positions, BN, Z, device, sms;
+  int V, max_rows, max_positions, BN, Z, device, sms, nslot;
   ss_dtype ldt, qdt;
   int grid1, grid2, grid3;
   size_t smem1, smem2, smem3;
@@ -88,7 +89,8 @@ ss_status ss_plan_create(ss_plan** out, int32_t V, int32_t max_rows, int32_t max
     return fail(SS_ERR_ARG, "need 1 <= max_rows <= max_positions <= 2^24");
   if ((logits_dtype != SS_F32 && logits_dtype != SS_BF16) || (q_dtype != SS_F32 && q_dtype != SS_BF16))
     return fail(SS_ERR_ARG, "dtype must be SS_F32 or SS_BF16");
-  if (tile != 0 && tile != 8192 && tile != 16384) return fail(SS_ERR_UNSUPPORTED, "tile must be 0, 8192 or 16384");
+  if (tile != 0 && tile != 4096 && tile != 8192 && tile != 16384)
+    return fail(SS_ERR_UNSUPPORTED, "tile must be 0, 4096, 8192 or 16384");
   int ndev = 0;
   cudaError_t e = cudaGetDeviceCount(&ndev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDeviceCount");
@@ -100,15 +102,24 @@ ss_status ss_plan_create(ss_plan** out, int32_t V, int32_t max_rows, int32_t max
   int smem_optin = 0;
   cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
 
+  int smem_sm = 0;
+  cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, device);
+
   const bool bf16 = logits_dtype == SS_BF16;
   int BN = tile;
   if (BN == 0) {
-    // 8192-token tiles keep two ring slots per CTA and two CTAs per SM in
-    // shared memory; larger vocabularies switch to 16384 when the stage-2
-    // merge of Z_v * 128 candidates would not fit.
-    BN = 8192;
-    if ((long long)ss::stage2_smem_bytes((V + BN - 1) / BN) > smem_optin) BN = 16384;
+    // 16 KB stages (4096 fp32 / 8192 bf16 tokens), larger only when the
+    // stage-2 merge of Z_v lists of 128 would not fit in shared memory
+    BN = bf16 ? 8192 : 4096;
+    while (BN < 16384 && (long long)ss::stage2_smem_bytes((V + BN - 1) / BN) > smem_optin) BN *= 2;
   }
+  // ring slots: as many as keep two CTAs per SM, else as many as fit one
+  int nslot = 0;
+  for (int s = ss::stage1_max_slots(); s >= 2 && nslot == 0; --s)
+    if (2 * ((long long)ss::stage1_smem_bytes(BN, bf16, s) + 1024) <= smem_sm) nslot = s;
+  for (int s = ss::stage1_max_slots(); s >= 2 && nslot == 0; --s)
+    if ((long long)ss::stage1_smem_bytes(BN, bf16, s) <= smem_optin) nslot = s;
+  if (nslot == 0) return fail(SS_ERR_UNSUPPORTED, "stage size too large for shared memory");
   ss_plan* p = new (std::nothrow) ss_plan();
   if (!p) return fail(SS_ERR_ARG, "out of host memory");
   p->V = V;
@@ -118,10 +129,11 @@ ss_status ss_plan_create(ss_plan** out, int32_t V, int32_t max_rows, int32_t max
   p->Z = (V + BN - 1) / BN;
   p->device = device;
   p->sms = sms;
+  p->nslot = nslot;
   p->ldt = logits_dtype;
   p->qdt = q_dtype;
-  p->k1 = ss::stage1_ptr(bf16, BN);
-  p->smem1 = ss::stage1_smem_bytes(BN, bf16, max_rows);
+  p->k1 = ss::stage1_ptr(bf16);
+  p->smem1 = ss::stage1_smem_bytes(BN, bf16, nslot);
   p->smem2 = ss::stage2_smem_bytes(p->Z);
   p->smem3 = ss::residual_smem_bytes(BN);
   if ((long long)p->smem2 > smem_optin || (long long)p->smem1 > smem_optin) {
@@ -169,6 +181,7 @@ void ss_plan_destroy(ss_plan* plan) { delete plan; }
 size_t ss_workspace_bytes(const ss_plan* p) { return p ? p->ws_bytes : 0; }
 int32_t ss_plan_tile(const ss_plan* p) { return p ? p->BN : 0; }
 int32_t ss_plan_num_tiles(const ss_plan* p) { return p ? p->Z : 0; }
+int32_t ss_plan_stage1_ctas(const ss_plan* p) { return p ? p->grid1 : 0; }
 size_t ss_workspace_diag_offset(const ss_plan* p) { return p ? p->off_diag : 0; }
 
 }  // extern "C"
@@ -204,6 +217,8 @@ ss_status fill_common(const ss_plan* pl, const ss_batch* b, const void* logits, 
   P.mask_words = (pl->V + 31) / 32;
   P.seeds = seeds;
   P.max_positions = pl->max_positions;
+  P.grid1 = pl->grid1;
+  P.nslot = pl->nslot;
   char* w = static_cast<char*>(b->workspace);
   P.ws.staging = reinterpret_cast<unsigned long long*>(w + pl->off_staging);
   P.ws.tile_lse = reinterpret_cast<float2*>(w + pl->off_tlse);
@@ -215,6 +230,13 @@ ss_status fill_common(const ss_plan* pl, const ss_batch* b, const void* logits, 
   P.ws.diag = reinterpret_cast<uint32_t*>(w + pl->off_diag);
   P.out = *out;
   return SS_OK;
+}
+
+// Grammar-mask rows start on 16-byte boundaries (so stage 1 bulk-copies the
+// words of each stage with its logits) when the array does and ceil(V/32) is
+// a multiple of 4.
+int mask_rows_copyable(const ss::Params& P) {
+  return P.bitmask != nullptr && aligned16(P.bitmask) && P.mask_words % 4 == 0 ? 1 : 0;
 }
 
 ss_status launch(const ss_plan* pl, const ss::Params& P, cudaStream_t st, bool verify, void* const* ev) {
@@ -232,7 +254,7 @@ ss_status launch(const ss_plan* pl, const ss::Params& P, cudaStream_t st, bool v
       e = cudaEventRecordWithFlags(static_cast<cudaEvent_t>(ev[i]), st, rec_flags);
   };
   rec(0);
-  ss::stage1_launch(pl->ldt == SS_BF16, pl->BN, pl->grid1, pl->smem1, st, P);
+  ss::stage1_launch(pl->ldt == SS_BF16, pl->grid1, pl->smem1, st, P);
   rec(1);
   ss::stage2_kernel<<<pl->grid2, ss::kNT, pl->smem2, st>>>(P, verify ? 1 : 0);
   rec(2);
@@ -261,6 +283,7 @@ ss_status ss_sample(const void* logits, const ss_batch* params, const int32_t* h
   P.history = history;
   P.bitmask = bitmask;
   P.bias = bias;
+  P.mask_tma = mask_rows_copyable(P);
   DeviceGuard guard(pl->device);
   return launch(pl, P, static_cast<cudaStream_t>(params->stream), false, params->events);
 }
@@ -284,6 +307,7 @@ ss_status ss_verify(const void* target_logits, const void* draft_probs, const in
   P.q = draft_probs;
   P.ld_q = params->ld_q;
   P.q_bf16 = pl->qdt == SS_BF16;
+  P.mask_tma = mask_rows_copyable(P);
   DeviceGuard guard(pl->device);
   return launch(pl, P, static_cast<cudaStream_t>(params->stream), true, params->events);
 }

@@ -35,9 +35,9 @@ struct ResidEntry {
 };
 
 struct Workspace {
-  unsigned long long* staging;   // [P * Z * 128] packed candidates
-  float2* tile_lse;              // [P * Z] (tile max, sum exp(x - max)) when requested
-  uint32_t* tile_status;         // [P * Z]
+  unsigned long long* staging;   // [P * Z * 128] packed candidates, one list per segment
+  float2* tile_lse;              // [P * Z] per segment (max, sum exp(x - max)) when requested
+  uint32_t* tile_status;         // [P * Z] per segment SS_ST_* bits
   PosResult* pos;                // [P]
   uint32_t* row_count;           // [R] positions of the row done (stage-2 arrivals)
   uint32_t* resid_count;         // [1] queued residual passes
@@ -66,6 +66,9 @@ struct Params {
   int q_bf16;
   const uint64_t* seeds;
   int max_positions;
+  int grid1;                // CTAs of the stage-1 launch (fixes the segment split)
+  int nslot;                // stage-1 ring slots
+  int mask_tma;             // bitmask rows can be bulk-copied (16-byte aligned rows)
   Workspace ws;
   ss_out out;
 };
@@ -222,6 +225,16 @@ __device__ __forceinline__ int find_row(const int32_t* cu, int B, int pos) {
 __device__ __forceinline__ int num_positions(const Params& P) {
   const int n = P.cu_draft ? (__ldg(P.cu_draft + P.B) + P.B) : P.B;
   return min(n, P.max_positions);
+}
+
+// Segment split shared by stage 1 and stage 2.  The T = npos * Z stages
+// (position-major) are cut into G = min(grid1, T) contiguous ranges; CTA c of
+// stage 1 owns stages [seg_start(c), seg_start(c + 1)), at least one each.
+__device__ __forceinline__ long long seg_start(long long c, long long T, long long G) { return c * T / G; }
+// The CTA whose range holds stage g: the largest c with seg_start(c) <= g.
+__device__ __forceinline__ int seg_cta(long long g, long long T, long long G) { return (int)(((g + 1) * G - 1) / T); }
+__device__ __forceinline__ long long seg_grid(const Params& P, long long T) {
+  return T < (long long)P.grid1 ? T : (long long)P.grid1;
 }
 
 // ------------------------------------------------------------------ block helpers

@@ -1,22 +1,45 @@
-// Stage 1 of the two-stage tile-aware top-k (SonicSampler 3.2, Fig. 1 top):
-// one work item per (target position, vocabulary tile of B_N tokens).  Each
-// item streams its tile once, applies the logits prelude (grammar mask,
-// penalties, bias, temperature) and writes only the tile's 128 best packed
-// candidates (key << 32 | ~token) to the staging buffer, plus a status word
-// and, for untruncated verify positions, (tile max, sum of exp(x - max)).
+// Stage 1 of the two-stage top-k (SonicSampler 3.2, Fig. 1 top): the logits
+// prelude (grammar mask, penalties, bias, temperature) fused with a local
+// top-128, every logit streamed from HBM once.
 //
-// Selection is exact under the order (processed logit descending, token
-// ascending).  GB300 design:
-//  - persistent CTAs of 256 threads; a two-slot shared-memory ring is filled
-//    by 1-D bulk copies (cp.async.bulk, completion counted on an mbarrier), so
-//    the next tile streams in from HBM while the current one is processed;
-//  - each thread holds E = B_N / 256 processed logits in registers;
-//  - a threshold tau with at least 128 tile elements at or above it comes
-//    from the per-thread maxima (the 16th largest maximum of each warp,
-//    minimum over the 8 warps), so typically ~2-3% of the tile survives into
-//    shared memory, where a 256-bin histogram select finishes exactly;
-//  - tiles with few finite values, NaN among few finite values, or very many
-//    survivors take an out-of-line radix select over the resident tile.
+// Work split.  Each target position's row is cut into Z_v stages of B_N
+// tokens; the npos * Z_v stages, position-major, are divided into
+// G = min(grid, npos * Z_v) nearly equal contiguous ranges, one per CTA.  The
+// part of a CTA's range inside one row is a segment, so a row has 1..Z_v
+// segments; each segment leaves its exact top-128 (packed key << 32 | ~token)
+// in the staging buffer and stage 2 merges a row's segments (seg_start /
+// seg_cta give both kernels the same split).  This generalises the pages'
+// one-list-per-tile: a list per run of tiles keeps the property stage 2 needs
+// (every element of the row's top-128 is in its own list's top-128) while the
+// selection work falls from once per tile to once per segment.
+//
+// Per CTA:
+//  - a ring of shared-memory slots is filled several stages ahead by bulk
+//    copies (cp.async.bulk completing on one mbarrier per slot): the stage's
+//    logits and, when the rows allow it, its grammar-mask words;
+//  - per segment, a candidate buffer and a cut with two invariants:
+//    (a) every element seen in the segment whose packed value is >= cut is
+//        in the buffer;
+//    (b) at least min(128, elements seen) buffer entries are >= cut.
+//    The segment's first stage takes the cut from the per-thread maxima (the
+//    16th largest of each warp's 32 maxima, minimum over the 8 warps, so 128
+//    maxima lie at or above it); afterwards a thread whose 16 elements all
+//    fall below the cut does only the prelude and a NaN-propagating running
+//    maximum, and the rare elements at or above it are appended.  When the
+//    buffer passes kCompactAt entries it is cut back to its exact top-128,
+//    which raises the cut;
+//  - history / draft / bias tokens need their count and bias entries, so they
+//    are kept out of that path: their exact values are computed from the
+//    staged logits and appended separately, listed per segment in a hash
+//    table, or for very long histories (and verify positions that need the
+//    full-vocabulary normaliser) in a per-stage count table;
+//  - what the fast path cannot certify (the buffer overflows within a stage,
+//    or the first stage's cut admits fewer than 128 elements: few finite
+//    values, NaN, penalised maxima) is rolled back and replaced by an exact
+//    radix select of the stage's top-128, after which the cut is raised to
+//    the stage's 128th value.  Both invariants survive every step.
+//  - the segment's NaN status and, for untruncated stochastic verify
+//    positions, (max, sum exp(x - max)) over the segment go beside the list.
 #include <type_traits>
 
 #include "ss_common.cuh"
@@ -26,31 +49,73 @@ namespace ss {
 namespace {
 
 constexpr int kSpinLimit = 1 << 22;  // bounded mbarrier wait (about a second)
-constexpr int kRowCache = 2048;     // rows whose position offsets stage 1 keeps in shared memory
-constexpr int kSide = 1024;         // penalised tokens per tile held in the side table (power of 2)
-constexpr int kBiasPre = 64;        // bias entries prefetched per item
+constexpr int kMaxSlots = 4;         // ring slots at most
+constexpr int kCap = 1024;           // candidate buffer entries
+constexpr int kCompactAt = 512;      // buffer fill that triggers a compaction (<= kCap - kK)
+constexpr int kHashBits = 10;
+constexpr int kHash = 1 << kHashBits;  // hash slots for a segment's history / bias tokens
+constexpr int kHashMax = 512;        // tokens a segment may list in the hash table
+constexpr int kBiasPre = 64;         // bias entries prefetched per segment
+constexpr int kPre = kNT;            // history / draft ids prefetched per segment
+constexpr int kPT = 16;              // elements per thread per chunk
+constexpr int kChunk = kPT * kNT;    // elements per chunk (a stage is 1..4 chunks)
+constexpr float kLog2e = 1.4426950408889634f;
+
+static_assert(kCompactAt <= kCap - kK, "a stage fallback appends 128 entries after the rollback");
+
+// One segment's row bookkeeping, copied with cp.async one segment ahead.
+struct __align__(16) RowBuf {
+  ss_bias_entry bias[kBiasPre];  // bias[r][e]      (e < min(bias_stride, kBiasPre))
+  int hist[kPre];                // history[r][h]   (h < min(hist_stride, kPre))
+  int draft[kPre];               // drafts of the row before this position (< min(j, kPre))
+  ss_row_params rp;
+  int pos, r, j, c0, c1;         // position, row, draft index, cu_draft[r], cu_draft[r + 1]
+  int pad[3];
+};
 
 struct __align__(16) S1Smem {
   SelectSmem sel;
-  unsigned long long mbar[2];
-  int cnt, nan_flag, out_cnt, nside;
-  float side[kSide];  // processed-before-temperature values of the tile's history / bias tokens
-  float tw[kNT / 32];
-  float wmax[kNT / 32];
+  unsigned long long mbar[kMaxSlots];
+  unsigned long long slots[kNT / 32];
+  unsigned long long cut;
   double red[kNT / 32];
+  float tw[kNT / 32];
+  float lm[kNT / 32];
+  int cnt[3];  // appends of stage k go to cnt[k % 3]
+  int dead, nan_flag, nf, out_cnt;
 };
 
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return (uint32_t)__cvta_generic_to_shared(p);
+struct Layout {
+  size_t ring, mask, cand, tmp, out, hkey, hval, ftok, finfo, sm, rb, total;
+};
+
+__host__ __device__ inline size_t up128(size_t x) { return (x + 127) & ~(size_t)127; }
+
+__host__ __device__ inline Layout layout(int BN, int esz, int nslot) {
+  Layout L;
+  size_t o = 0;
+  L.ring = o;  o = up128(o + (size_t)nslot * BN * esz);
+  L.mask = o;  o = up128(o + (size_t)nslot * (BN / 8));
+  L.cand = o;  o = up128(o + (size_t)kCap * 8);
+  L.tmp = o;   o = up128(o + ((size_t)kCap * 8 > (size_t)BN * 2 ? (size_t)kCap * 8 : (size_t)BN * 2));
+  L.out = o;   o = up128(o + (size_t)kK * 8);
+  L.hkey = o;  o = up128(o + (size_t)kHash * 4);
+  L.hval = o;  o = up128(o + (size_t)kHash * 4);
+  L.ftok = o;  o = up128(o + (size_t)kHashMax * 4);
+  L.finfo = o; o = up128(o + (size_t)kHashMax * 4);
+  L.sm = o;    o = up128(o + sizeof(S1Smem));
+  L.rb = o;    o = up128(o + 2 * sizeof(RowBuf));
+  L.total = o;
+  return L;
 }
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
 __device__ __forceinline__ void mbar_init(unsigned long long* m) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(m)) : "memory");
 }
 
-// One bulk copy global -> shared whose bytes complete on the slot's mbarrier.
-__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, unsigned long long* m) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(m)), "r"(bytes) : "memory");
+__device__ __forceinline__ void bulk_copy(void* dst, const void* src, uint32_t bytes, unsigned long long* m) {
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
                ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(m))
                : "memory");
@@ -67,6 +132,18 @@ __device__ __forceinline__ bool mbar_wait(unsigned long long* m, uint32_t parity
     if (ok) return true;
   }
   return false;
+}
+
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// max that returns NaN if either operand is NaN
+__device__ __forceinline__ float fmax_nan(float a, float b) {
+  float d;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+  return d;
 }
 
 template <bool BF16>
@@ -86,73 +163,98 @@ __device__ __forceinline__ float vec_elem(const uint4& v, int jj) {
   }
 }
 
-struct TileCtx {
-  int t0, nt, need, pos, r, j;
-  bool mask_on, aux_on;
-  bool side;  // aux entries are side-table indices + 1 (else count | bias flag)
-  const ss_bias_entry* brow;
-};
-
-// Processed logit of tile element li (the same fp32 steps as the fast path).
-// Penalties and bias commute with the mask (a masked token ends at -inf either
-// way), so a history / bias token's value may be taken from the side table
-// before the mask is applied.
-template <bool BF16>
-__device__ __forceinline__ float proc_elem(const Params& P, const RowCtx& rc, const TileCtx& tc,
-                                           const unsigned char* ring, const uint16_t* aux, const float* side,
-                                           int li) {
-  float v = raw_at<BF16>(ring, li);
-  const int tok = tc.t0 + li;
-  if (tc.aux_on) {
-    const uint32_t a = aux[li];
-    if (a != 0u) {
-      if (tc.side) v = side[a - 1];
-      else v = apply_penalty_bias(v, a & 0x7FFFu, (a & 0x8000u) != 0u, tok, rc, tc.brow);
-    }
-  }
-  if (tc.mask_on) {
-    const uint32_t w = __ldg(P.bitmask + (size_t)tc.pos * P.mask_words + (tok >> 5));
-    if (((w >> (tok & 31)) & 1u) == 0u) v = -INFINITY;
-  }
-  v = __fmul_rn(v, rc.rT);
-  return v;
+// Stage element li of chunk ch for vector v, lane element jj: vectors of a
+// chunk are kNT apart so that each load is one coalesced 16-byte access.
+template <int VEC>
+__device__ __forceinline__ int elem_index(int ch, int v, int jj) {
+  constexpr int NV = kPT / VEC;
+  return ((ch * NV + v) * kNT + (int)threadIdx.x) * VEC + jj;
 }
 
-// Exact tile top-`need` for the cases the fast path leaves out (few finite
-// values, NaN among them, or more survivors than fit in shared memory):
-// MSB-first radix select on the 32-bit keys of the resident tile, then the
-// lowest tokens among elements equal to the boundary key.  Thread t owns the
-// contiguous elements [t*E, t*E + E), so token order is (thread, element).
-template <bool BF16, int E>
-__device__ __noinline__ void generic_select(const Params& P, const RowCtx& rc, const TileCtx& tc,
-                                            const unsigned char* ring, const uint16_t* aux, S1Smem& sm,
-                                            unsigned long long* stg) {
+// Everything the out-of-line paths need to recompute a stage element's
+// processed value, by value (nothing of the hot loop's state is addressed).
+struct StageCtx {
+  const unsigned char* ring;
+  const uint32_t* msl;           // the stage's mask words (shared or global), or null
+  const ss_bias_entry* bl;       // the row's bias list (shared copy when it fits)
+  const int* hkey;
+  const uint32_t* hval;
+  const uint16_t* aux;
+  RowCtx rc;
+  int t0, nt;
+  bool hashed, staged;
+};
+
+__device__ __forceinline__ uint32_t hash_of(int tok) { return ((uint32_t)tok * 0x9E3779B1u) >> (32 - kHashBits); }
+
+// Slot of token tok in the segment's hash table, or -1.
+__device__ __forceinline__ int hash_find(const int* hkey, int tok) {
+  uint32_t h = hash_of(tok);
+  for (int probe = 0; probe < kHash; ++probe) {
+    const int k = hkey[h];
+    if (k == tok) return (int)h;
+    if (k == -1) return -1;
+    h = (h + 1) & (kHash - 1);
+  }
+  return -1;
+}
+
+// History count (bits 0..30) and bias flag (bit 31) of stage element li.
+__device__ __forceinline__ uint32_t flag_info(const StageCtx& s, int li) {
+  if (s.hashed) {
+    const int h = hash_find(s.hkey, s.t0 + li);
+    return h >= 0 ? s.hval[h] : 0u;
+  }
+  if (s.staged) {
+    const uint32_t a = s.aux[li];
+    return (a & 0x7FFFu) | ((a & 0x8000u) << 16);
+  }
+  return 0u;
+}
+
+// Processed value of stage element li with history count / bias flag `info`
+// (the prelude's fp32 steps in order: mask, penalties, bias, temperature).
+template <bool BF16>
+__device__ __forceinline__ float value_with(const StageCtx& s, int li, uint32_t info) {
+  float v = raw_at<BF16>(s.ring, li);
+  if (s.msl && ((s.msl[li >> 5] >> (li & 31)) & 1u) == 0u) v = -INFINITY;
+  if (info) v = apply_penalty_bias(v, info & 0x7FFFFFFFu, (info >> 31) != 0u, s.t0 + li, s.rc, s.bl);
+  return __fmul_rn(v, s.rc.rT);
+}
+
+// Exact top-`need` of the stage, appended to cand[cbase + *acnt]: MSB-first
+// radix select on the 32-bit keys, then the lowest tokens among elements equal
+// to the boundary key.  Thread t owns the contiguous elements [t*E, t*E + E)
+// so that token order is (thread, element).  Sets sm.nan_flag on NaN.
+template <bool BF16>
+__device__ __noinline__ void stage_exact(const StageCtx& s, S1Smem& sm, int* acnt, int cbase, unsigned long long* cand,
+                                         int need, int E) {
   const int tid = threadIdx.x, lane = tid & 31;
   const int base = tid * E;
   auto key_of = [&](int li) -> uint32_t {
-    if (li >= tc.nt) return 0u;  // not a token of this tile
-    const float v = proc_elem<BF16>(P, rc, tc, ring, aux, sm.side, li);
+    const float v = value_with<BF16>(s, li, flag_info(s, li));
     return (v != v) ? kKeyNegInf : f2key(v);
   };
   bool nan_seen = false;
   for (int k = 0; k < E; ++k) {
     const int li = base + k;
-    if (li < tc.nt) {
-      const float v = proc_elem<BF16>(P, rc, tc, ring, aux, sm.side, li);
+    if (li < s.nt) {
+      const float v = value_with<BF16>(s, li, flag_info(s, li));
       nan_seen |= (v != v);
     }
   }
   if (nan_seen) sm.nan_flag = 1;
   uint32_t prefix = 0u, pmask = 0u;
-  int rem = tc.need;
+  int rem = need;
   for (int d = 0; d < 4; ++d) {
     const int shift = 24 - 8 * d;
     sm.sel.hist[tid & 255] = 0u;
     __syncthreads();
     for (int k = 0; k < E; ++k) {
       const int li = base + k;
-      const uint32_t key = key_of(li);
-      const bool match = li < tc.nt && ((key & pmask) == prefix);
+      const bool in = li < s.nt;
+      const uint32_t key = in ? key_of(li) : 0u;
+      const bool match = in && ((key & pmask) == prefix);
       const uint32_t bin = match ? ((key >> shift) & 255u) : 256u;
       const uint32_t peers = __match_any_sync(0xffffffffu, bin);
       if (match && lane == __ffs(peers) - 1) atomicAdd(&sm.sel.hist[bin], (uint32_t)__popc(peers));
@@ -168,11 +270,11 @@ __device__ __noinline__ void generic_select(const Params& P, const RowCtx& rc, c
   int ties = 0;
   for (int k = 0; k < E; ++k) {
     const int li = base + k;
-    if (li >= tc.nt) continue;
+    if (li >= s.nt) continue;
     const uint32_t key = key_of(li);
     if (key > kstar) {
-      const int s = atomicAdd(&sm.out_cnt, 1);
-      if (s < kK) stg[s] = pack(key, (uint32_t)(tc.t0 + li));
+      const int q = cbase + atomicAdd(acnt, 1);
+      if (q < kCap) cand[q] = pack(key, (uint32_t)(s.t0 + li));
     } else if (key == kstar) {
       ++ties;
     }
@@ -182,448 +284,554 @@ __device__ __noinline__ void generic_select(const Params& P, const RowCtx& rc, c
   int rank = incl - ties;
   for (int k = 0; k < E && rank < rem; ++k) {
     const int li = base + k;
-    if (li >= tc.nt) continue;
+    if (li >= s.nt) continue;
     if (key_of(li) == kstar) {
-      const int s = atomicAdd(&sm.out_cnt, 1);
-      if (s < kK) stg[s] = pack(kstar, (uint32_t)(tc.t0 + li));
+      const int q = cbase + atomicAdd(acnt, 1);
+      if (q < kCap) cand[q] = pack(kstar, (uint32_t)(s.t0 + li));
       ++rank;
     }
   }
+  __syncthreads();
+}
+
+// Exact top-`need` of cand[0..n) (distinct values) to emit(); lo / hi are the
+// smallest and largest entries, found here.  All threads call.
+template <class Emit>
+__device__ __forceinline__ void select_top(unsigned long long* cand, unsigned long long* tmp, int n, int need,
+                                           S1Smem& sm, Emit emit) {
+  unsigned long long mn = ~0ull, mx = 0ull;
+  for (int i = threadIdx.x; i < n; i += kNT) {
+    const unsigned long long c = cand[i];
+    mn = c < mn ? c : mn;
+    mx = c > mx ? c : mx;
+  }
+  const unsigned long long lo = block_min_u64(mn, sm.slots);
+  const unsigned long long hi = block_max_u64(mx, sm.slots);
+  block_select(cand, tmp, n, need, lo, hi, sm.sel, emit);
+}
+
+// Cut the buffer back to its exact top-128; returns the new cut (the 128th).
+__device__ __noinline__ unsigned long long compact(unsigned long long* cand, unsigned long long* tmp,
+                                                   unsigned long long* outb, int n, S1Smem& sm) {
+  if (threadIdx.x == 0) sm.out_cnt = 0;
+  __syncthreads();
+  select_top(cand, tmp, n, kK, sm, [&](unsigned long long c) {
+    const int q = atomicAdd(&sm.out_cnt, 1);
+    if (q < kK) outb[q] = c;
+  });
+  const int t = threadIdx.x;
+  const unsigned long long c = t < kK ? outb[t] : ~0ull;
+  if (t < kK) cand[t] = c;
+  return block_min_u64(c, sm.slots);
+}
+
+// Load chunk ch of the stage and apply mask and temperature; returns the
+// NaN-propagating maximum.  MASK: msl holds the stage's mask words (shared or
+// global memory).  FULL: the stage has B_N tokens (otherwise elements past
+// the last token read as -inf and are never appended).
+template <bool BF16, bool MASK, bool FULL>
+__device__ __forceinline__ float load_chunk(const unsigned char* ring, const uint32_t* msl, float rT, int ch, int nt,
+                                            float (&x)[kPT]) {
+  constexpr int VEC = BF16 ? 8 : 4;
+  constexpr int NV = kPT / VEC;
+  float m = -INFINITY;
+#pragma unroll
+  for (int v = 0; v < NV; ++v) {
+    const int e0 = elem_index<VEC>(ch, v, 0);
+    const uint4 raw = *reinterpret_cast<const uint4*>(ring + (size_t)e0 * (BF16 ? 2 : 4));
+    uint32_t bits = 0xFFFFFFFFu;
+    if constexpr (MASK) bits = (FULL || e0 < nt) ? msl[e0 >> 5] >> (e0 & 31) : 0u;
+#pragma unroll
+    for (int jj = 0; jj < VEC; ++jj) {
+      float val = vec_elem<BF16>(raw, jj);
+      if constexpr (MASK) {
+        if (((bits >> jj) & 1u) == 0u) val = -INFINITY;
+      }
+      val = __fmul_rn(val, rT);
+      if (!FULL && e0 + jj >= nt) val = -INFINITY;
+      x[v * VEC + jj] = val;
+      m = fmax_nan(m, val);
+    }
+  }
+  return m;
+}
+
+template <bool BF16>
+__device__ __forceinline__ float load_chunk_sel(bool mask, bool full, const unsigned char* ring, const uint32_t* msl,
+                                                float rT, int ch, int nt, float (&x)[kPT]) {
+  if (mask)
+    return full ? load_chunk<BF16, true, true>(ring, msl, rT, ch, nt, x)
+                : load_chunk<BF16, true, false>(ring, msl, rT, ch, nt, x);
+  return full ? load_chunk<BF16, false, true>(ring, msl, rT, ch, nt, x)
+              : load_chunk<BF16, false, false>(ring, msl, rT, ch, nt, x);
+}
+
+// The value the stream computes for stage element li (mask and temperature:
+// the same fp32 steps as load_chunk, so the same bits).
+template <bool BF16>
+__device__ __forceinline__ float stream_value(const unsigned char* ring, const uint32_t* msl, float rT, int li) {
+  float v = raw_at<BF16>(ring, li);
+  if (msl && ((msl[li >> 5] >> (li & 31)) & 1u) == 0u) v = -INFINITY;
+  return __fmul_rn(v, rT);
+}
+
+// Running (max, sum exp(x - max)) of one thread; -inf (and NaN) terms add nothing.
+__device__ __forceinline__ void lse_add(float& M, float& S, float v) {
+  if (!(v > -INFINITY)) return;
+  const float Mn = fmaxf(M, v);
+  S = S * exp2f((M - Mn) * kLog2e) + exp2f((v - Mn) * kLog2e);
+  M = Mn;
 }
 
 }  // namespace
 
-// One work item's bookkeeping besides its tile, copied into shared memory with
-// cp.async one item ahead (no registers held while the copies are in flight).
-template <int MW>
-struct __align__(16) NextBuf {
-  ss_bias_entry bias[kBiasPre];  // bias[r][t]        (t < min(bias_stride, kBiasPre))
-  int hist[kNT];            // history[r][t]          (t < hist_stride)
-  int draft[kNT];           // drafts of the row      (t < min(j, gamma))
-  uint32_t mask[MW];        // the tile's bitmask words
-  ss_row_params rp;
-  int pos, r, j, gamma;     // the item's target position, row, draft index, row draft count
-};
-
-__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
-
-template <bool BF16, int NCH>
+template <bool BF16>
 __global__ void __launch_bounds__(kNT, 2) stage1_kernel(const Params P) {
-  constexpr int VEC = BF16 ? 8 : 4;
-  constexpr int E = NCH * VEC;
-  constexpr int BN = kNT * E;
   constexpr int ESZ = BF16 ? 2 : 4;
-  constexpr int MW = BN / 32;
-  using Bits = typename std::conditional<(E > 32), unsigned long long, uint32_t>::type;
+  constexpr int VEC = BF16 ? 8 : 4;
+  constexpr int NV = kPT / VEC;
   extern __shared__ __align__(128) unsigned char smem_raw[];
-  // [ring slot 0 | ring slot 1 | aux (uint16 per token; the select's scratch
-  //  afterwards) | survivors | S1Smem | NextBuf x 2 | row offsets]
-  unsigned char* ring0 = smem_raw;
-  uint16_t* aux = reinterpret_cast<uint16_t*>(smem_raw + 2 * BN * ESZ);
-  unsigned long long* tmp = reinterpret_cast<unsigned long long*>(aux);
-  unsigned long long* surv = reinterpret_cast<unsigned long long*>(smem_raw + 2 * BN * ESZ + BN * 2);
-  S1Smem& sm = *reinterpret_cast<S1Smem*>(smem_raw + 2 * BN * ESZ + BN * 2 + kCap1 * 8);
-  NextBuf<MW>* nbuf = reinterpret_cast<NextBuf<MW>*>(smem_raw + 2 * BN * ESZ + BN * 2 + kCap1 * 8 + sizeof(S1Smem));
-  int* offs = reinterpret_cast<int*>(reinterpret_cast<unsigned char*>(nbuf) + 2 * sizeof(NextBuf<MW>));
-  static_assert(BN * 2 >= kCap1 * 8, "aux region must hold the select scratch");
-  static_assert(sizeof(S1Smem) % 16 == 0 && sizeof(NextBuf<MW>) % 16 == 0, "16-byte regions");
+  const int BN = P.BN, NS = P.nslot;
+  const Layout L = layout(BN, ESZ, NS);
+  unsigned char* ring0 = smem_raw + L.ring;
+  uint32_t* mask0 = reinterpret_cast<uint32_t*>(smem_raw + L.mask);
+  unsigned long long* cand = reinterpret_cast<unsigned long long*>(smem_raw + L.cand);
+  unsigned long long* tmp = reinterpret_cast<unsigned long long*>(smem_raw + L.tmp);
+  uint16_t* aux = reinterpret_cast<uint16_t*>(smem_raw + L.tmp);  // per-stage count table (shares tmp)
+  unsigned long long* outb = reinterpret_cast<unsigned long long*>(smem_raw + L.out);
+  int* hkey = reinterpret_cast<int*>(smem_raw + L.hkey);
+  uint32_t* hval = reinterpret_cast<uint32_t*>(smem_raw + L.hval);
+  int* ftok = reinterpret_cast<int*>(smem_raw + L.ftok);
+  uint32_t* finfo = reinterpret_cast<uint32_t*>(smem_raw + L.finfo);
+  S1Smem& sm = *reinterpret_cast<S1Smem*>(smem_raw + L.sm);
+  RowBuf* rb = reinterpret_cast<RowBuf*>(smem_raw + L.rb);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int V = P.V, Z = P.Z;
   if (blockIdx.x == 0 && tid == 0) *P.ws.resid_count = 0u;  // residual queue of this call
   const int npos = num_positions(P);
-  const long long total = (long long)npos * Z;
-  // first target position of each row (cu_draft[r] + r), cached for the row lookups
-  const bool cached = P.cu_draft != nullptr && P.B + 1 <= kRowCache;
-  if (cached)
-    for (int q = tid; q <= P.B; q += kNT) offs[q] = __ldg(P.cu_draft + q) + q;
+  const long long T = (long long)npos * Z;
+  if (T <= 0) return;
+  const long long G = seg_grid(P, T);
+  if ((long long)blockIdx.x >= G) return;
+  const long long g0 = seg_start(blockIdx.x, T, G), g1 = seg_start(blockIdx.x + 1, T, G);
+  const bool mask_tma = P.mask_tma != 0 && P.bitmask != nullptr;
+  const int nch = BN / kChunk;
 
-  auto issue = [&](long long it, int slot) {  // thread 0 only
-    const int pos = (int)(it / Z);
-    const int t0 = (int)(it - (long long)pos * Z) * BN;
+  // thread 0: bulk copies of stage g (logits, then the mask words) into a slot
+  auto issue = [&](long long g, int slot) {
+    const int pos = (int)(g / Z);
+    const int t0 = (int)(g - (long long)pos * Z) * BN;
     const int nt = min(BN, V - t0);
     const uint32_t bytes = (uint32_t)((nt * ESZ + 15) & ~15);
-    const unsigned char* src = static_cast<const unsigned char*>(P.logits) + ((size_t)pos * P.ld + t0) * ESZ;
-    bulk_load(ring0 + slot * BN * ESZ, src, bytes, &sm.mbar[slot]);
+    const uint32_t mbytes = mask_tma ? (uint32_t)((((nt + 31) >> 5) * 4 + 15) & ~15) : 0u;
+    unsigned long long* mb = &sm.mbar[slot];
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(mb)), "r"(bytes + mbytes)
+                 : "memory");
+    bulk_copy(ring0 + (size_t)slot * BN * ESZ,
+              static_cast<const unsigned char*>(P.logits) + ((size_t)pos * P.ld + t0) * ESZ, bytes, mb);
+    if (mask_tma) bulk_copy(mask0 + (size_t)slot * (BN / 32), P.bitmask + (size_t)pos * P.mask_words + (t0 >> 5), mbytes, mb);
   };
-  // row of a work item (every thread, from the cached offsets)
-  auto locate = [&](long long it, int& pos, int& r, int& j, int& gamma) {
-    pos = (int)(it / Z);
-    r = pos;
-    j = 0;
-    gamma = 0;
-    if (P.cu_draft) {
-      int lo = 0, hi = P.B - 1;
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        const int o = cached ? offs[mid] : (__ldg(P.cu_draft + mid) + mid);
-        if (o <= pos) lo = mid; else hi = mid - 1;
-      }
-      r = lo;
-      const int c0 = cached ? offs[lo] - lo : __ldg(P.cu_draft + lo);
-      const int c1 = cached ? offs[lo + 1] - lo - 1 : __ldg(P.cu_draft + lo + 1);
-      j = pos - c0 - r;
-      gamma = c1 - c0;
-    }
-  };
-  // warp 0: locate an item's row and copy its bookkeeping into nb with
-  // cp.async (the other warps never wait on these loads)
-  auto prefetch = [&](long long it, NextBuf<MW>& nb) {
-    int pos, r, j, gamma;
-    locate(it, pos, r, j, gamma);
+  // warp 0: a position's row bookkeeping into nb (cp.async; c1 too when c1src is set)
+  auto prefetch = [&](int pos, int r, int c0, int c1, const int32_t* c1src, RowBuf& nb) {
+    const int j = P.cu_draft ? pos - c0 - r : 0;
     if (lane == 0) {
       nb.pos = pos;
       nb.r = r;
       nb.j = j;
-      nb.gamma = gamma;
+      nb.c0 = c0;
+      if (c1src) cp_async4(&nb.c1, c1src);
+      else nb.c1 = c1;
     }
-    const int t0 = (int)(it - (long long)pos * Z) * BN;
-    const int nt = min(BN, V - t0);
     if (lane < (int)(sizeof(ss_row_params) / 4))
       cp_async4(reinterpret_cast<uint32_t*>(&nb.rp) + lane, reinterpret_cast<const uint32_t*>(P.rows + r) + lane);
     if (P.history != nullptr)
-      for (int q = lane; q < min(P.hist_stride, kNT); q += 32)
+      for (int q = lane; q < min(P.hist_stride, kPre); q += 32)
         cp_async4(&nb.hist[q], P.history + (size_t)r * P.hist_stride + q);
-    if (P.cu_draft != nullptr) {
-      const int base = cached ? offs[r] - r : __ldg(P.cu_draft + r);
-      for (int q = lane; q < min(min(j, gamma), kNT); q += 32) cp_async4(&nb.draft[q], P.draft_ids + base + q);
-    }
+    if (P.cu_draft != nullptr)
+      for (int q = lane; q < min(j, kPre); q += 32) cp_async4(&nb.draft[q], P.draft_ids + c0 + q);
     if (P.bias != nullptr)
       for (int q = lane; q < min(P.bias_stride, kBiasPre); q += 32) {  // 4-byte copies: 4-byte aligned entries
         const ss_bias_entry* be = P.bias + (size_t)r * P.bias_stride + q;
         cp_async4(&nb.bias[q].token, &be->token);
         cp_async4(&nb.bias[q].value, &be->value);
       }
-    if (P.bitmask != nullptr)
-      for (int w = lane; w < MW && w * 32 < nt; w += 32)
-        cp_async4(&nb.mask[w], P.bitmask + (size_t)pos * P.mask_words + (t0 >> 5) + w);
     asm volatile("cp.async.commit_group;" ::: "memory");
+  };
+  // staging list of position pos for this CTA's segment
+  auto slot_of = [&](int pos) -> size_t {
+    const long long gs = (long long)pos * Z;
+    return (size_t)gs + (size_t)((long long)blockIdx.x - seg_cta(gs, T, G));
   };
 
   if (tid == 0) {
-    mbar_init(&sm.mbar[0]);
-    mbar_init(&sm.mbar[1]);
+    sm.dead = 0;
+    for (int s = 0; s < NS; ++s) mbar_init(&sm.mbar[s]);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    sm.cnt = 0;
-    sm.nan_flag = 0;
-    sm.out_cnt = 0;
-    sm.nside = 0;
-    if ((long long)blockIdx.x < total) issue(blockIdx.x, 0);
+    for (int s = 0; s < NS && g0 + s < g1; ++s) issue(g0 + s, s);
   }
-  __syncthreads();  // offsets cached, barriers initialised
-  if (warp == 0 && (long long)blockIdx.x < total) prefetch(blockIdx.x, nbuf[0]);
+  if (warp == 0) {
+    const int pos = (int)(g0 / Z);
+    int r = pos, c0 = 0, c1 = 0;
+    if (P.cu_draft) {
+      r = find_row(P.cu_draft, P.B, pos);
+      c0 = __ldg(P.cu_draft + r);
+      c1 = __ldg(P.cu_draft + r + 1);
+    }
+    prefetch(pos, r, c0, c1, nullptr, rb[0]);
+  }
   cp_async_wait_all();
   __syncthreads();
 
-  int k = 0;
-  for (long long item = blockIdx.x; item < total; item += gridDim.x, ++k) {
-    const int slot = k & 1;
-    const unsigned char* ring = ring0 + slot * BN * ESZ;
-    const NextBuf<MW>& cb = nbuf[slot];
-    const long long nx = item + gridDim.x;
-    // prefetch the next item: its tile into the other ring slot and its
-    // bookkeeping into the other buffer (both freed by the previous item's
-    // final barrier)
-    if (nx < total && warp == 0) {
-      if (lane == 0) {
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        issue(nx, slot ^ 1);
-      }
-      prefetch(nx, nbuf[slot ^ 1]);
-    }
-    const int pos = cb.pos, r = cb.r, j = cb.j, gamma = cb.gamma;
-
-    const int tile = (int)(item - (long long)pos * Z);
-    TileCtx tc;
-    tc.pos = pos;
-    tc.t0 = tile * BN;
-    tc.nt = min(BN, V - tc.t0);
-    tc.need = min(kK, tc.nt);
-    tc.r = r;
-    tc.j = j;
+  long long g = g0;
+  int kst = 0;  // stages consumed by this CTA: slot kst % NS, phase (kst / NS) & 1
+  int buf = 0;
+  bool dead = false;
+  while (g < g1 && !dead) {
+    const RowBuf& cb = rb[buf];
+    const int pos = cb.pos, r = cb.r, j = cb.j;
+    const int gamma = P.cu_draft ? cb.c1 - cb.c0 : 0;
+    const long long gs = (long long)pos * Z;
+    const long long ge = min(g1, gs + Z);
+    const size_t lslot = slot_of(pos);
     const RowCtx rc = make_row(cb.rp, P.hist_stride, P.bias_stride);
-    tc.mask_on = (rc.flags & SS_MASK) && P.bitmask != nullptr;
+    // the next segment's bookkeeping (the next position; rows own consecutive positions)
+    if (warp == 0 && ge < g1) {
+      const int pn = pos + 1;
+      if (P.cu_draft && pn >= cb.c1 + r + 1) prefetch(pn, r + 1, cb.c1, 0, P.cu_draft + r + 2, rb[buf ^ 1]);
+      else if (P.cu_draft) prefetch(pn, r, cb.c0, cb.c1, nullptr, rb[buf ^ 1]);
+      else prefetch(pn, pn, 0, 0, nullptr, rb[buf ^ 1]);
+    }
+
+    const int seg_lo = (int)(g - gs) * BN, seg_hi = min(V, (int)(ge - gs) * BN);
+    const bool mask_on = (rc.flags & SS_MASK) && P.bitmask != nullptr;
     const bool pen_on = (rc.flags & SS_PENALTY) && P.history != nullptr;
     const bool bias_on = (rc.flags & SS_BIAS) && P.bias != nullptr;
-    tc.aux_on = pen_on || bias_on;
-    tc.brow = bias_on ? P.bias + (size_t)r * P.bias_stride : nullptr;
-    unsigned long long* stg = P.ws.staging + (size_t)item * kK;
-    const int t0 = tc.t0, nt = tc.nt;
-    const bool full = (nt == BN);
+    const int jn = P.cu_draft ? min(j, gamma) : 0;
+    const bool lse_on = P.cu_draft != nullptr && j < gamma && rc.stoch && !rc.trunc;
+    const bool aux_on = rc.valid && (pen_on || bias_on);
+    const int nflag = (pen_on ? rc.hist_len + jn : 0) + (bias_on ? rc.n_bias : 0);
+    const bool hashed = aux_on && !lse_on && nflag <= kHashMax;
+    const bool staged = aux_on && !hashed;
+    const ss_bias_entry* brow = bias_on ? P.bias + (size_t)r * P.bias_stride : nullptr;
+    const ss_bias_entry* bl = (bias_on && rc.n_bias <= kBiasPre) ? cb.bias : brow;
 
-    // the tile's bytes
-    const bool landed = mbar_wait(&sm.mbar[slot], (uint32_t)((k >> 1) & 1));
-    if (!__syncthreads_and(landed)) {
-      // a bulk copy did not complete: record it and stop this CTA
-      if (tid == 0) {
-        atomicAdd(P.ws.diag + 3, 1u);
-        if (nx < total) mbar_wait(&sm.mbar[slot ^ 1], (uint32_t)(((k + 1) >> 1) & 1));
-      }
-      cp_async_wait_all();
-      break;
+    // ---- segment set-up: counters and the hash table of flagged tokens
+    if (tid == 0) {
+      sm.cnt[0] = sm.cnt[1] = sm.cnt[2] = 0;
+      sm.nan_flag = 0;
+      sm.nf = 0;
     }
-
-    // tile-local history counts and bias flags
-    tc.side = tc.aux_on && (pen_on ? rc.hist_len + min(j, gamma) : 0) + (bias_on ? rc.n_bias : 0) <= kSide;
-    if (tc.aux_on && rc.valid) {
-      uint4* a4 = reinterpret_cast<uint4*>(aux);
-      for (int w = tid; w < BN / 8; w += kNT) a4[w] = make_uint4(0u, 0u, 0u, 0u);
-      __syncthreads();
-      uint32_t* a32 = reinterpret_cast<uint32_t*>(aux);
-      auto count = [&](int id) {
-        if (id >= t0 && id < t0 + nt) atomicAdd(a32 + ((id - t0) >> 1), 1u << (16 * ((id - t0) & 1)));
+    if (hashed)
+      for (int q = tid; q < kHash; q += kNT) {
+        hkey[q] = -1;
+        hval[q] = 0u;
+      }
+    __syncthreads();
+    if (hashed) {
+      auto insert = [&](int tok, uint32_t add, uint32_t orv) {
+        if (tok < seg_lo || tok >= seg_hi) return;  // also drops padding (< 0) and ids >= V
+        uint32_t h = hash_of(tok);
+        for (int probe = 0; probe < kHash; ++probe) {
+          const int old = atomicCAS(&hkey[h], -1, tok);
+          if (old == -1 || old == tok) {
+            if (add) atomicAdd(&hval[h], add);
+            if (orv) atomicOr(&hval[h], orv);
+            return;
+          }
+          h = (h + 1) & (kHash - 1);
+        }
       };
       if (pen_on) {
-        if (tid < rc.hist_len) count(cb.hist[tid]);
         const int32_t* hrow = P.history + (size_t)r * P.hist_stride;
-        for (int h = tid + kNT; h < rc.hist_len; h += kNT) count(__ldg(hrow + h));
-        if (P.cu_draft) {  // drafts accepted before this verify position
-          if (tid < min(j, gamma)) count(cb.draft[tid]);
-          const int base = __ldg(P.cu_draft + r);
-          for (int q = tid + kNT; q < min(j, gamma); q += kNT) count(__ldg(P.draft_ids + base + q));
-        }
+        for (int h = tid; h < rc.hist_len; h += kNT) insert(h < kPre ? cb.hist[h] : __ldg(hrow + h), 1u, 0u);
+        for (int s = tid; s < jn; s += kNT) insert(s < kPre ? cb.draft[s] : __ldg(P.draft_ids + cb.c0 + s), 1u, 0u);
       }
-      if (bias_on) {
-        auto flag = [&](int id) {
-          if (id >= t0 && id < t0 + nt) atomicOr(a32 + ((id - t0) >> 1), 0x8000u << (16 * ((id - t0) & 1)));
-        };
-        if (tid < min(rc.n_bias, kBiasPre)) flag(cb.bias[tid].token);
-        for (int e = kBiasPre + tid; e < rc.n_bias; e += kNT) flag(tc.brow[e].token);
-      }
+      if (bias_on)
+        for (int e = tid; e < rc.n_bias; e += kNT) insert(e < kBiasPre ? cb.bias[e].token : brow[e].token, 0u, 0x80000000u);
       __syncthreads();
-      if (tc.side) {
-        // penalised values of the flagged tokens, computed here (few live
-        // registers) so the hot loop only looks them up; each thread handles
-        // the tokens it owns in the hot loop's layout, so no barrier is needed
-        for (int c = 0; c < NCH; ++c) {
-          const int e0 = (c * kNT + tid) * VEC;
-          if (e0 >= nt) break;
-          uint32_t w[VEC / 2];
-          if constexpr (BF16) {
-            const uint4 a = *reinterpret_cast<const uint4*>(aux + e0);
-            w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
+      for (int q = tid; q < kHash; q += kNT)
+        if (hkey[q] >= 0) {
+          const int i = atomicAdd(&sm.nf, 1);
+          ftok[i] = hkey[q];
+          finfo[i] = hval[q];
+        }
+      __syncthreads();
+    }
+    const int nf = hashed ? sm.nf : 0;
+
+    unsigned long long cutp = 0ull;  // packed cut (0: everything)
+    int n = 0;                       // buffer entries (uniform; read between barriers)
+    float lM = -INFINITY, lS = 0.0f; // this thread's running (max, sum exp) for the normaliser
+    bool first = true;
+
+    for (; g < ge; ++g, ++kst, first = false) {
+      const int slot = kst % NS;
+      const unsigned char* ring = ring0 + (size_t)slot * BN * ESZ;
+      const int t0 = (int)(g - gs) * BN;
+      const int nt = min(BN, V - t0);
+      const bool full = nt == BN;
+      const uint32_t* msl = nullptr;
+      if (mask_on) msl = mask_tma ? mask0 + (size_t)slot * (BN / 32) : P.bitmask + (size_t)pos * P.mask_words + (t0 >> 5);
+      int* acnt = &sm.cnt[kst % 3];
+      // the next stage's counter was last read after the barrier two stages back
+      if (tid == 0) sm.cnt[(kst + 1) % 3] = 0;
+      // a copy that never lands is noticed by all threads after the stage barrier
+      if (!mbar_wait(&sm.mbar[slot], (uint32_t)((kst / NS) & 1))) sm.dead = 1;
+
+      StageCtx sc;
+      sc.ring = ring;
+      sc.msl = msl;
+      sc.bl = bl;
+      sc.hkey = hkey;
+      sc.hval = hval;
+      sc.aux = aux;
+      sc.rc = rc;
+      sc.t0 = t0;
+      sc.nt = nt;
+      sc.hashed = hashed;
+      sc.staged = staged;
+
+      if (rc.valid) {
+        // per-stage count table (long histories, normaliser positions)
+        if (staged) {
+          uint4* a4 = reinterpret_cast<uint4*>(aux);
+          for (int w = tid; w < BN / 8; w += kNT) a4[w] = make_uint4(0u, 0u, 0u, 0u);
+          __syncthreads();
+          uint32_t* a32 = reinterpret_cast<uint32_t*>(aux);
+          auto count = [&](int id) {
+            if (id >= t0 && id < t0 + nt) atomicAdd(a32 + ((id - t0) >> 1), 1u << (16 * ((id - t0) & 1)));
+          };
+          if (pen_on) {
+            const int32_t* hrow = P.history + (size_t)r * P.hist_stride;
+            for (int h = tid; h < rc.hist_len; h += kNT) count(h < kPre ? cb.hist[h] : __ldg(hrow + h));
+            for (int s = tid; s < jn; s += kNT) count(s < kPre ? cb.draft[s] : __ldg(P.draft_ids + cb.c0 + s));
+          }
+          if (bias_on)
+            for (int e = tid; e < rc.n_bias; e += kNT) {
+              const int id = e < kBiasPre ? cb.bias[e].token : brow[e].token;
+              if (id >= t0 && id < t0 + nt) atomicOr(a32 + ((id - t0) >> 1), 0x8000u << (16 * ((id - t0) & 1)));
+            }
+          __syncthreads();
+        }
+        auto append = [&](unsigned long long pk) {
+          const int q = n + atomicAdd(acnt, 1);
+          if (q < kCap) cand[q] = pk;
+        };
+
+        // pass 0 (a segment's first stage only): the cut from the per-thread
+        // maxima; pass 1: the stream (prelude, running maximum, rare appends)
+        bool nan_seen = false;
+        for (int pass = first ? 0 : 1; pass < 2; ++pass) {
+          const uint32_t ck = pk_key(cutp);
+          const float cut_f = ck <= kKeyNegInf ? -INFINITY : key2f(ck);
+          float mt = -INFINITY;
+          for (int ch = 0; ch < nch; ++ch) {
+            float x[kPT];
+            const float m = load_chunk_sel<BF16>(mask_on, full, ring, msl, rc.rT, ch, nt, x);
+            if (pass == 0) {
+#pragma unroll
+              for (int e = 0; e < kPT; ++e) mt = fmaxf(mt, x[e]);
+              continue;
+            }
+            if (!(m < cut_f)) {
+              // elements at or above the cut (or NaN): re-derived from the slot
+              uint32_t bits = 0u;
+#pragma unroll
+              for (int e = 0; e < kPT; ++e) bits |= (x[e] < cut_f ? 0u : 1u) << e;
+              while (bits) {
+                const int e = __ffs((int)bits) - 1;
+                bits &= bits - 1u;
+                const int li = ((ch * NV + e / VEC) * kNT + tid) * VEC + e % VEC;
+                if (!full && li >= nt) continue;
+                const float xv = stream_value<BF16>(ring, msl, rc.rT, li);
+                const bool isn = xv != xv;
+                nan_seen |= isn;
+                const unsigned long long pk = pack(isn ? kKeyNegInf : f2key(xv), (uint32_t)(t0 + li));
+                if (pk >= cutp && !(aux_on && flag_info(sc, li) != 0u)) append(pk);
+              }
+            }
+            if (lse_on) {
+              float mc = -INFINITY;
+#pragma unroll
+              for (int e = 0; e < kPT; ++e) {
+                const int li = elem_index<VEC>(ch, e / VEC, e % VEC);
+                if (staged && (full || li < nt) && aux[li] != 0u) x[e] = -INFINITY;  // added with its exact value
+                mc = fmaxf(mc, x[e]);
+              }
+              if (mc > -INFINITY) {
+                const float Mn = fmaxf(lM, mc);
+                const float off = Mn * kLog2e;
+                float s = 0.0f;
+#pragma unroll
+                for (int e = 0; e < kPT; ++e)
+                  if (x[e] > -INFINITY) s += exp2f(__fmaf_rn(x[e], kLog2e, -off));
+                lS = lS * exp2f((lM - Mn) * kLog2e) + s;
+                lM = Mn;
+              }
+            }
+          }
+          if (pass == 0) {
+            // 16th largest of the warp's 32 maxima (bitonic sort across lanes);
+            // tau = the minimum over warps, so >= 8 * 16 elements are >= tau
+            float v = mt;
+#pragma unroll
+            for (int kk = 2; kk <= 32; kk <<= 1) {
+#pragma unroll
+              for (int d = kk >> 1; d > 0; d >>= 1) {
+                const float o = __shfl_xor_sync(0xffffffffu, v, d);
+                const bool keep_max = (((lane & d) == 0) == ((lane & kk) == 0));
+                v = keep_max ? fmaxf(v, o) : fminf(v, o);
+              }
+            }
+            if (lane == 15) sm.tw[warp] = v;
+            __syncthreads();
+            float tau = sm.tw[0];
+#pragma unroll
+            for (int w = 1; w < kNT / 32; ++w) tau = fminf(tau, sm.tw[w]);
+            cutp = pack(f2key(tau), 0xFFFFFFFFu);  // every element >= tau
+          }
+        }
+
+        // ---- flagged tokens of this stage, with their exact values
+        auto flagged = [&](int li, uint32_t info) {
+          const float v = value_with<BF16>(sc, li, info);
+          const bool isn = v != v;
+          nan_seen |= isn;
+          if (lse_on) lse_add(lM, lS, v);
+          const unsigned long long pk = pack(isn ? kKeyNegInf : f2key(v), (uint32_t)(t0 + li));
+          if (pk >= cutp) append(pk);
+        };
+        if (hashed) {
+          for (int i = tid; i < nf; i += kNT) {
+            const int li = ftok[i] - t0;
+            if (li >= 0 && li < nt) flagged(li, finfo[i]);
+          }
+        } else if (staged) {
+          const uint4* a4 = reinterpret_cast<const uint4*>(aux);
+          for (int w = tid; w < BN / 8; w += kNT) {
+            const uint4 a = a4[w];
             if ((a.x | a.y | a.z | a.w) == 0u) continue;
-          } else {
-            const uint2 a = *reinterpret_cast<const uint2*>(aux + e0);
-            w[0] = a.x; w[1] = a.y;
-            if ((a.x | a.y) == 0u) continue;
-          }
-          for (int jj = 0; jj < VEC; ++jj) {
-            const uint32_t a = (w[jj >> 1] >> (16 * (jj & 1))) & 0xFFFFu;
-            if (a == 0u) continue;
-            const int li = e0 + jj;
-            const float pv = apply_penalty_bias(raw_at<BF16>(ring, li), a & 0x7FFFu, (a & 0x8000u) != 0u, t0 + li,
-                                                rc, tc.brow);
-            const int q = atomicAdd(&sm.nside, 1);  // < kSide: bounded by the flagged-token count
-            sm.side[q] = pv;
-            aux[li] = (uint16_t)(q + 1);
-          }
-        }
-      }
-    }
-
-    if (!rc.valid) {  // invalid row parameters: stage 2 reports the row, nothing to select
-      for (int q = tid; q < kK; q += kNT) stg[q] = 0ull;
-      if (tid == 0) P.ws.tile_status[item] = 0u;
-    } else {
-      // ---- prelude in registers, per-thread maximum -----------------------------
-      float x[E];
-      float m = -INFINITY;
-      if (full && !tc.mask_on && !tc.aux_on) {
-#pragma unroll
-        for (int c = 0; c < NCH; ++c) {
-          const uint4 raw = *reinterpret_cast<const uint4*>(ring + (size_t)(c * kNT + tid) * 16);
-#pragma unroll
-          for (int jj = 0; jj < VEC; ++jj) {
-            const float v = __fmul_rn(vec_elem<BF16>(raw, jj), rc.rT);
-            x[c * VEC + jj] = v;
-            m = fmaxf(m, v);
-          }
-        }
-      } else {
-        // general case: grammar mask and history / bias tokens; FULL drops the
-        // ragged-tile check from full tiles
-        auto hot = [&](auto full_c) {
-          constexpr bool FULL = decltype(full_c)::value;
-#pragma unroll
-          for (int c = 0; c < NCH; ++c) {
-            const int e0 = (c * kNT + tid) * VEC;
-            const uint4 raw = *reinterpret_cast<const uint4*>(ring + (size_t)(c * kNT + tid) * 16);
-            const uint32_t mwc = (tc.mask_on && (FULL || e0 < nt)) ? cb.mask[e0 >> 5] : 0xFFFFFFFFu;
-            uint32_t auxw[VEC / 2];
-            bool any_aux = false;
-            if (tc.aux_on && (FULL || e0 < nt)) {
-              if constexpr (BF16) {
-                const uint4 a = *reinterpret_cast<const uint4*>(aux + e0);
-                auxw[0] = a.x; auxw[1] = a.y; auxw[2] = a.z; auxw[3] = a.w;
-                any_aux = (a.x | a.y | a.z | a.w) != 0u;
-              } else {
-                const uint2 a = *reinterpret_cast<const uint2*>(aux + e0);
-                auxw[0] = a.x; auxw[1] = a.y;
-                any_aux = (a.x | a.y) != 0u;
-              }
-            }
-#pragma unroll
-            for (int jj = 0; jj < VEC; ++jj) {
-              float v = vec_elem<BF16>(raw, jj);
-              if (any_aux) {
-                const uint32_t a = (auxw[jj >> 1] >> (16 * (jj & 1))) & 0xFFFFu;
-                if (a != 0u) v = sm.side[(a - 1) & (kSide - 1)];
-              }
-              if (((mwc >> ((e0 + jj) & 31)) & 1u) == 0u) v = -INFINITY;
-              v = __fmul_rn(v, rc.rT);
-              if (!FULL && e0 + jj >= nt) v = -INFINITY;
-              x[c * VEC + jj] = v;
-              m = fmaxf(m, v);
+            const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
+            for (int q = 0; q < 8; ++q) {
+              const uint32_t h = (aw[q >> 1] >> (16 * (q & 1))) & 0xFFFFu;
+              const int li = w * 8 + q;
+              if (h != 0u && li < nt) flagged(li, (h & 0x7FFFu) | ((h & 0x8000u) << 16));
             }
           }
-        };
-        if (full) hot(std::true_type{});
-        else hot(std::false_type{});
-      }
-
-      // ---- threshold from the per-thread maxima ----------------------------------
-      // Warp bitonic sort (descending) of the 32 maxima; lane 15 holds the 16th
-      // largest.  tau = min over warps, so >= 8 * 16 = 128 threads have a
-      // maximum >= tau, i.e. >= 128 tile elements are >= tau.
-      {
-        float v = m;
-#pragma unroll
-        for (int kk = 2; kk <= 32; kk <<= 1) {
-#pragma unroll
-          for (int d = kk >> 1; d > 0; d >>= 1) {
-            const float o = __shfl_xor_sync(0xffffffffu, v, d);
-            const bool keep_max = (((lane & d) == 0) == ((lane & kk) == 0));
-            v = keep_max ? fmaxf(v, o) : fminf(v, o);
-          }
         }
-        if (lane == 15) sm.tw[warp] = v;
-        if (lane == 0) sm.wmax[warp] = v;
-      }
-      if (tid == 0) {  // per-item counters (last read before the previous item's final barrier)
-        sm.cnt = 0;
-        sm.nan_flag = 0;
-        sm.out_cnt = 0;
+        if (nan_seen) sm.nan_flag = 1;
       }
       __syncthreads();
-      float tau = sm.tw[0], tmax = sm.wmax[0];
-#pragma unroll
-      for (int w = 1; w < kNT / 32; ++w) {
-        tau = fminf(tau, sm.tw[w]);
-        tmax = fmaxf(tmax, sm.wmax[w]);
+      if (sm.dead) {
+        dead = true;
+        break;
       }
+      // read between this barrier and the next stage's appends, which use another counter
+      int n_end = n + *acnt;
 
-      // ---- (tile max, sum exp) for untruncated stochastic verify positions -----
-      if (P.cu_draft != nullptr && j < gamma && rc.stoch && !rc.trunc) {
-        float sum = 0.0f;
-        if (tmax > -INFINITY) {
-          const float k2 = 1.4426950408889634f;
-          const float off = tmax * k2;
-#pragma unroll
-          for (int e = 0; e < E; ++e) {
-            const float v = x[e];
-            if (v > -INFINITY) sum += exp2f(__fmaf_rn(v, k2, -off));
-          }
+      // ---- fallback: the buffer overflowed, or the first stage's cut certified too few
+      const int need_s = min(kK, nt);
+      if (rc.valid && (n_end > kCap || (first && n_end < need_s))) {
+        __syncthreads();  // every thread has read the counter
+        if (tid == 0) {
+          *acnt = 0;  // roll this stage's appends back
+          atomicAdd(P.ws.diag + 0, 1u);
         }
-        const double S = block_sum_d((double)sum, sm.red);
-        if (tid == 0) P.ws.tile_lse[item] = make_float2(tmax, (float)S);
-      }
-
-      // ---- survivors: x >= tau (tau = -inf: every finite value) -----------------
-      // A bitmask per thread, one shared-memory reservation per warp; survivors
-      // are re-derived from the resident tile (same fp32 steps; a survivor is
-      // never masked).  NaN compares false and so survives; it is keyed as -inf
-      // and reported.
-      const bool few_finite = !(tau > -INFINITY);
-      const float tcut = few_finite ? -3.402823466e38f : tau;
-      Bits bits = 0;
-#pragma unroll
-      for (int e = 0; e < E; ++e)
-        if (!(x[e] < tcut)) bits |= (Bits)1 << e;
-      const int cnt = (E > 32) ? __popcll((unsigned long long)bits) : __popc((uint32_t)bits);
-      int incl = cnt;
-#pragma unroll
-      for (int d = 1; d < 32; d <<= 1) {
-        const int o = __shfl_up_sync(0xffffffffu, incl, d);
-        if (lane >= d) incl += o;
-      }
-      int wbase = 0;
-      if (lane == 31 && incl > 0) wbase = atomicAdd(&sm.cnt, incl);
-      wbase = __shfl_sync(0xffffffffu, wbase, 31);
-      int off = wbase + incl - cnt;
-      while (bits) {
-        const int e = (E > 32) ? (__ffsll((long long)bits) - 1) : (__ffs((int)(uint32_t)bits) - 1);
-        bits &= bits - 1;
-        const int li = ((e / VEC) * kNT + tid) * VEC + (e % VEC);
-        float v = raw_at<BF16>(ring, li);
-        if (tc.aux_on) {
-          const uint32_t a = aux[li];
-          if (a != 0u) v = sm.side[(a - 1) & (kSide - 1)];
-        }
-        v = __fmul_rn(v, rc.rT);
-        const bool isn = (v != v);
-        if (isn) sm.nan_flag = 1;
-        if (off < kCap1) surv[off] = pack(isn ? kKeyNegInf : f2key(v), (uint32_t)(t0 + li));
-        ++off;
-      }
-      __syncthreads();
-      const int n = sm.cnt;
-      const bool nan_here = sm.nan_flag != 0;
-      auto emit = [&](unsigned long long cv) {
-        const int q = atomicAdd(&sm.out_cnt, 1);
-        if (q < kK) stg[q] = cv;
-      };
-      // few finite values: the fast path is exact only with enough of them and no NaN
-      if (n <= kCap1 && n >= tc.need && !(few_finite && nan_here) && (tc.side || !tc.aux_on)) {
-        const unsigned long long lo = nan_here ? pack(kKeyNegInf, 0xFFFFFFFFu) : pack(f2key(tcut), 0xFFFFFFFFu);
-        const unsigned long long hi = pack(f2key(tmax), 0u);
-        block_select(surv, tmp, n, tc.need, lo, hi, sm.sel, emit);
-      } else {
-        if (tid == 0) atomicAdd(P.ws.diag + 0, 1u);
-        if (tid == 0) sm.out_cnt = 0;
         __syncthreads();
-        generic_select<BF16, E>(P, rc, tc, ring, aux, sm, stg);
+        stage_exact<BF16>(sc, sm, acnt, n, cand, need_s, BN / kNT);
+        const int added = min(*acnt, need_s);  // need_s unless the keys disagreed between passes
+        unsigned long long mn = ~0ull;
+        for (int i = n + tid; i < n + added; i += kNT) mn = cand[i] < mn ? cand[i] : mn;
+        mn = block_min_u64(mn, sm.slots);
+        const unsigned long long base_cut = first ? 0ull : cutp;
+        // a stage of >= 128 tokens: nothing outside its top-128 is >= its 128th value
+        cutp = (nt >= kK && added == need_s && mn > base_cut) ? mn : base_cut;
+        n_end = n + added;
       }
-      __syncthreads();
-      // empty slots: a tile with fewer than 128 tokens (or any slot the select
-      // left unwritten) holds the sentinel 0
-      for (int q = min(sm.out_cnt, tc.need) + tid; q < kK; q += kNT) stg[q] = 0ull;
-      if (tid == 0) P.ws.tile_status[item] = sm.nan_flag ? SS_ST_NAN : 0u;
+      // refill this slot with the stage NS ahead (every read of it is done)
+      if (tid == 0 && g + NS < g1) {
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        issue(g + NS, slot);
+      }
+      // ---- keep room in the buffer: exact top-128, which raises the cut
+      if (rc.valid && n_end > kCompactAt) {
+        cutp = compact(cand, tmp, outb, n_end, sm);
+        n_end = kK;
+      }
+      n = n_end;
     }
-    if (tid == 0) sm.nside = 0;  // read by this item's hot loop only
-    cp_async_wait_all();  // the next item's bookkeeping
+    if (dead) break;
+
+    // ---- segment end: the exact top-128 of the buffer goes to staging
+    unsigned long long* stg = P.ws.staging + lslot * kK;
+    if (rc.valid) {
+      const int need = min(kK, seg_hi - seg_lo);
+      if (tid == 0) sm.out_cnt = 0;
+      __syncthreads();
+      select_top(cand, tmp, n, need, sm, [&](unsigned long long c) {
+        const int q = atomicAdd(&sm.out_cnt, 1);
+        if (q < kK) stg[q] = c;
+      });
+      for (int q = min(sm.out_cnt, need) + tid; q < kK; q += kNT) stg[q] = 0ull;
+      if (tid == 0) P.ws.tile_status[lslot] = sm.nan_flag ? SS_ST_NAN : 0u;
+      if (lse_on) {
+        float Mb = lM;
+#pragma unroll
+        for (int d = 16; d > 0; d >>= 1) Mb = fmaxf(Mb, __shfl_xor_sync(0xffffffffu, Mb, d));
+        if (lane == 0) sm.lm[warp] = Mb;
+        __syncthreads();
+        Mb = sm.lm[0];
+#pragma unroll
+        for (int w = 1; w < kNT / 32; ++w) Mb = fmaxf(Mb, sm.lm[w]);
+        const double part = (lM > -INFINITY) ? (double)lS * (double)exp2f((lM - Mb) * kLog2e) : 0.0;
+        const double S = block_sum_d(part, sm.red);
+        if (tid == 0) P.ws.tile_lse[lslot] = make_float2(Mb, (float)S);
+      }
+    } else {  // invalid row parameters: stage 2 reports the row
+      for (int q = tid; q < kK; q += kNT) stg[q] = 0ull;
+      if (tid == 0) P.ws.tile_status[lslot] = 0u;
+    }
+    cp_async_wait_all();  // the next segment's bookkeeping
+    __syncthreads();
+    buf ^= 1;
+  }
+
+  if (dead) {
+    // A bulk copy did not complete within the wait limit: count it, leave
+    // empty lists for this and the remaining positions of the range, and let
+    // the copies still in flight land (bounded waits) before the CTA exits.
+    if (tid == 0) atomicAdd(P.ws.diag + 3, 1u);
+    const int p_first = (int)(g / Z), p_last = (int)((g1 - 1) / Z);
+    for (int p = p_first; p <= p_last; ++p) {
+      const size_t ls = slot_of(p);
+      for (int q = tid; q < kK; q += kNT) P.ws.staging[ls * kK + q] = 0ull;
+      if (tid == 0) {
+        P.ws.tile_status[ls] = 0u;
+        P.ws.tile_lse[ls] = make_float2(-INFINITY, 0.0f);
+      }
+    }
+    if (tid == 0)
+      for (int s = 0; s < NS && g + s < g1; ++s) mbar_wait(&sm.mbar[(kst + s) % NS], (uint32_t)(((kst + s) / NS) & 1));
+    cp_async_wait_all();
     __syncthreads();
   }
 }
 
-// Explicit instantiations: fp32 / bf16 logits, B_N = 8192 and 16384.
-template __global__ void stage1_kernel<false, 8>(const Params);
-template __global__ void stage1_kernel<false, 16>(const Params);
-template __global__ void stage1_kernel<true, 4>(const Params);
-template __global__ void stage1_kernel<true, 8>(const Params);
+template __global__ void stage1_kernel<false>(const Params);
+template __global__ void stage1_kernel<true>(const Params);
 
-const void* stage1_ptr(bool bf16, int BN) {
-  if (!bf16) return BN == 8192 ? (const void*)stage1_kernel<false, 8> : (const void*)stage1_kernel<false, 16>;
-  return BN == 8192 ? (const void*)stage1_kernel<true, 4> : (const void*)stage1_kernel<true, 8>;
+const void* stage1_ptr(bool bf16) {
+  return bf16 ? (const void*)stage1_kernel<true> : (const void*)stage1_kernel<false>;
 }
 
-void stage1_launch(bool bf16, int BN, int grid, size_t smem, cudaStream_t st, const Params& P) {
-  if (!bf16) {
-    if (BN == 8192) stage1_kernel<false, 8><<<grid, kNT, smem, st>>>(P);
-    else stage1_kernel<false, 16><<<grid, kNT, smem, st>>>(P);
-  } else {
-    if (BN == 8192) stage1_kernel<true, 4><<<grid, kNT, smem, st>>>(P);
-    else stage1_kernel<true, 8><<<grid, kNT, smem, st>>>(P);
-  }
+void stage1_launch(bool bf16, int grid, size_t smem, cudaStream_t st, const Params& P) {
+  if (bf16) stage1_kernel<true><<<grid, kNT, smem, st>>>(P);
+  else stage1_kernel<false><<<grid, kNT, smem, st>>>(P);
 }
 
-size_t stage1_smem_bytes(int BN, bool bf16, int max_rows) {
-  const size_t nb = BN == 8192 ? sizeof(NextBuf<256>) : sizeof(NextBuf<512>);
-  return (size_t)2 * BN * (bf16 ? 2 : 4) + (size_t)BN * 2 + (size_t)kCap1 * 8 + sizeof(S1Smem) + 2 * nb +
-         (max_rows + 1 <= kRowCache ? (size_t)(max_rows + 1) * 4 : 0);
-}
+size_t stage1_smem_bytes(int BN, bool bf16, int nslot) { return layout(BN, bf16 ? 2 : 4, nslot).total; }
+
+int stage1_max_slots() { return kMaxSlots; }
 
 }  // namespace ss

@@ -3,9 +3,10 @@
 // "Rejection Sampler").
 //
 // One work item per target position (persistent CTAs of 256 threads):
-//  1. merge: the position's Z_v tiles each left 128 packed candidates in the
-//     staging buffer.  tau2 = the largest "smallest kept candidate" of a full
-//     tile certifies 128 candidates, so only packed values >= tau2 enter
+//  1. merge: each of the position's segments (1..Z_v runs of tiles, one per
+//     stage-1 CTA) left its top-128 packed candidates in the staging buffer.
+//     tau2 = the largest "smallest kept candidate" of a full list certifies
+//     128 candidates, so only packed values >= tau2 enter
 //     shared memory, and a histogram select picks the exact top-128, which a
 //     bitonic network then sorts (processed logit descending, token ascending).
 //  2. epilogue (dl-note Combination): fp64 softmax over the candidates,
@@ -126,6 +127,9 @@ __global__ void __launch_bounds__(kNT) stage2_kernel(const Params P, int verify)
     const int r = sm.r, j = sm.j, gamma = sm.gamma;
     const RowCtx rc = make_row(P.rows[r], P.hist_stride, P.bias_stride);
     const uint32_t position = rc.position + (uint32_t)j;
+    // the position's segment lists (the stage-1 split of the npos * Z stages)
+    const long long T = (long long)npos * Z, G = seg_grid(P, T);
+    const int nseg = seg_cta((long long)pos * Z + Z - 1, T, G) - seg_cta((long long)pos * Z, T, G) + 1;
     const uint64_t seed = P.seeds[r];
     const bool is_draft = verify && j >= 0 && j < gamma;
     int32_t* cid = P.out.cand_ids ? P.out.cand_ids + (size_t)pos * kK : nullptr;
@@ -161,13 +165,13 @@ __global__ void __launch_bounds__(kNT) stage2_kernel(const Params P, int verify)
       // largest such minimum bounds the position's top-128 from below.
       const size_t tbase = (size_t)pos * Z;
       uint32_t tst = 0u;
-      for (int t = tid; t < Z; t += kNT) tst |= P.ws.tile_status[tbase + t];
+      for (int t = tid; t < nseg; t += kNT) tst |= P.ws.tile_status[tbase + t];
       if (tst) atomicOr(&sm.status, tst);
       const unsigned long long* stg = P.ws.staging + tbase * kK;
-      for (int i = tid; i < cap; i += kNT) tmp[i] = stg[i];
+      for (int i = tid; i < nseg * kK; i += kNT) tmp[i] = stg[i];
       __syncthreads();
       unsigned long long tm = 0ull;
-      for (int t = tid >> 5; t < Z; t += kNT / 32) {
+      for (int t = tid >> 5; t < nseg; t += kNT / 32) {
         unsigned long long mn = ~0ull;
 #pragma unroll
         for (int q = 0; q < kK / 32; ++q) {
@@ -179,7 +183,7 @@ __global__ void __launch_bounds__(kNT) stage2_kernel(const Params P, int verify)
       }
       const unsigned long long tau2 = block_max_u64(tm, sm.slots);
       unsigned long long lmin = ~0ull, lmax = 0ull;
-      for (int i = tid; i < cap; i += kNT) {
+      for (int i = tid; i < nseg * kK; i += kNT) {
         const unsigned long long c = tmp[i];
         if (c != 0ull && c >= tau2) {
           cand[atomicAdd(&sm.cnt, 1)] = c;
@@ -304,9 +308,9 @@ __global__ void __launch_bounds__(kNT) stage2_kernel(const Params P, int verify)
             // full-vocabulary softmax: LSE from the tiles' (max, sum exp) partials
             if (tid == 0) {
               float M = -INFINITY;
-              for (int tt = 0; tt < Z; ++tt) M = fmaxf(M, P.ws.tile_lse[(size_t)pos * Z + tt].x);
+              for (int tt = 0; tt < nseg; ++tt) M = fmaxf(M, P.ws.tile_lse[(size_t)pos * Z + tt].x);
               double S = 0.0;
-              for (int tt = 0; tt < Z; ++tt) {
+              for (int tt = 0; tt < nseg; ++tt) {
                 const float2 ms = P.ws.tile_lse[(size_t)pos * Z + tt];
                 if (ms.x > -INFINITY) S += (double)ms.y * exp((double)ms.x - (double)M);
               }

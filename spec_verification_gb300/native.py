@@ -47,7 +47,7 @@ class Out(C.Structure):
 
 
 EXPORTS = ["ss_plan_create", "ss_plan_destroy", "ss_workspace_bytes", "ss_plan_tile",
-           "ss_plan_num_tiles", "ss_sample", "ss_verify", "ss_status_str", "ss_last_error",
+           "ss_plan_num_tiles", "ss_plan_stage1_ctas", "ss_sample", "ss_verify", "ss_status_str", "ss_last_error",
            "ss_workspace_diag_offset", "ss_sample_noalloc"]
 
 _lib = None
@@ -74,6 +74,8 @@ def library() -> C.CDLL:
     L.ss_plan_tile.restype = C.c_int32
     L.ss_plan_num_tiles.argtypes = [C.c_void_p]
     L.ss_plan_num_tiles.restype = C.c_int32
+    L.ss_plan_stage1_ctas.argtypes = [C.c_void_p]
+    L.ss_plan_stage1_ctas.restype = C.c_int32
     L.ss_sample.argtypes = [C.c_void_p, C.POINTER(Batch), C.c_void_p, C.c_void_p, C.c_void_p,
                             C.c_void_p, C.POINTER(Out)]
     L.ss_sample.restype = C.c_int
@@ -109,6 +111,7 @@ class Plan:
         self.logits_dtype, self.q_dtype = logits_dtype, q_dtype
         self.tile = L.ss_plan_tile(self._p)
         self.num_tiles = L.ss_plan_num_tiles(self._p)
+        self.stage1_ctas = L.ss_plan_stage1_ctas(self._p)
         self.workspace_bytes = L.ss_workspace_bytes(self._p)
         self.diag_offset = L.ss_workspace_diag_offset(self._p)
 

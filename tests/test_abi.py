@@ -15,7 +15,7 @@ HEADER = ROOT / "include" / "ss.h"
 def header_functions():
     text = HEADER.read_text()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\**\s*(ss_[a-z_]+)\s*\(", text, flags=re.M)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\**\s*(ss_[a-z0-9_]+)\s*\(", text, flags=re.M)
     return sorted(set(names))
 
 
