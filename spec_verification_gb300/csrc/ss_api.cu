@@ -108,9 +108,9 @@ ss_status ss_plan_create(ss_plan** out, int32_t V, int32_t max_rows, int32_t max
   const bool bf16 = logits_dtype == SS_BF16;
   int BN = tile;
   if (BN == 0) {
-    // 16 KB stages (4096 fp32 / 8192 bf16 tokens), larger only when the
-    // stage-2 merge of Z_v lists of 128 would not fit in shared memory
-    BN = bf16 ? 8192 : 4096;
+    // 8192-token stages, larger only when the stage-2 merge of Z_v lists of
+    // 128 would not fit in shared memory
+    BN = 8192;
     while (BN < 16384 && (long long)ss::stage2_smem_bytes((V + BN - 1) / BN) > smem_optin) BN *= 2;
   }
   // ring slots: as many as keep two CTAs per SM, else as many as fit one

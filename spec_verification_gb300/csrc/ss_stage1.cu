@@ -29,10 +29,12 @@
 //    buffer passes kCompactAt entries it is cut back to its exact top-128,
 //    which raises the cut;
 //  - history / draft / bias tokens need their count and bias entries, so they
-//    are kept out of that path: their exact values are computed from the
-//    staged logits and appended separately, listed per segment in a hash
-//    table, or for very long histories (and verify positions that need the
-//    full-vocabulary normaliser) in a per-stage count table;
+//    are kept out of that path: per segment they are listed in a hash table
+//    (which the rare appends consult) and their exact values, read straight
+//    from HBM, are the segment's first candidates; very long histories (and
+//    verify positions that need the full-vocabulary normaliser) use a
+//    per-stage count table instead, appending those tokens as their stage
+//    streams through;
 //  - what the fast path cannot certify (the buffer overflows within a stage,
 //    or the first stage's cut admits fewer than 128 elements: few finite
 //    values, NaN, penalised maxima) is rolled back and replaced by an exact
@@ -231,17 +233,20 @@ __device__ __noinline__ void stage_exact(const StageCtx& s, S1Smem& sm, int* acn
                                          int need, int E) {
   const int tid = threadIdx.x, lane = tid & 31;
   const int base = tid * E;
-  auto key_of = [&](int li) -> uint32_t {
-    const float v = value_with<BF16>(s, li, flag_info(s, li));
-    return (v != v) ? kKeyNegInf : f2key(v);
+  // hash mode: the listed tokens are candidates already and take no part
+  auto key_of = [&](int li, uint32_t& key) -> bool {
+    if (li >= s.nt) return false;
+    if (s.hashed && hash_find(s.hkey, s.t0 + li) >= 0) return false;
+    const float v = value_with<BF16>(s, li, s.staged ? flag_info(s, li) : 0u);
+    key = (v != v) ? kKeyNegInf : f2key(v);
+    return true;
   };
   bool nan_seen = false;
   for (int k = 0; k < E; ++k) {
     const int li = base + k;
-    if (li < s.nt) {
-      const float v = value_with<BF16>(s, li, flag_info(s, li));
-      nan_seen |= (v != v);
-    }
+    if (li >= s.nt || (s.hashed && hash_find(s.hkey, s.t0 + li) >= 0)) continue;
+    const float v = value_with<BF16>(s, li, s.staged ? flag_info(s, li) : 0u);
+    nan_seen |= (v != v);
   }
   if (nan_seen) sm.nan_flag = 1;
   uint32_t prefix = 0u, pmask = 0u;
@@ -251,9 +256,8 @@ __device__ __noinline__ void stage_exact(const StageCtx& s, S1Smem& sm, int* acn
     sm.sel.hist[tid & 255] = 0u;
     __syncthreads();
     for (int k = 0; k < E; ++k) {
-      const int li = base + k;
-      const bool in = li < s.nt;
-      const uint32_t key = in ? key_of(li) : 0u;
+      uint32_t key = 0u;
+      const bool in = key_of(base + k, key);
       const bool match = in && ((key & pmask) == prefix);
       const uint32_t bin = match ? ((key >> shift) & 255u) : 256u;
       const uint32_t peers = __match_any_sync(0xffffffffu, bin);
@@ -269,9 +273,9 @@ __device__ __noinline__ void stage_exact(const StageCtx& s, S1Smem& sm, int* acn
   const uint32_t kstar = prefix;
   int ties = 0;
   for (int k = 0; k < E; ++k) {
+    uint32_t key;
     const int li = base + k;
-    if (li >= s.nt) continue;
-    const uint32_t key = key_of(li);
+    if (!key_of(li, key)) continue;
     if (key > kstar) {
       const int q = cbase + atomicAdd(acnt, 1);
       if (q < kCap) cand[q] = pack(key, (uint32_t)(s.t0 + li));
@@ -283,9 +287,9 @@ __device__ __noinline__ void stage_exact(const StageCtx& s, S1Smem& sm, int* acn
   const int incl = block_inclusive_scan(ties, sm.sel.scan, &total);
   int rank = incl - ties;
   for (int k = 0; k < E && rank < rem; ++k) {
+    uint32_t key;
     const int li = base + k;
-    if (li >= s.nt) continue;
-    if (key_of(li) == kstar) {
+    if (key_of(li, key) && key == kstar) {
       const int q = cbase + atomicAdd(acnt, 1);
       if (q < kCap) cand[q] = pack(kstar, (uint32_t)(s.t0 + li));
       ++rank;
@@ -350,9 +354,17 @@ __device__ __forceinline__ float load_chunk(const unsigned char* ring, const uin
       val = __fmul_rn(val, rT);
       if (!FULL && e0 + jj >= nt) val = -INFINITY;
       x[v * VEC + jj] = val;
-      m = fmax_nan(m, val);
     }
   }
+  // NaN-propagating maximum as a tree (depth 4, not a chain of 16)
+  float t8[kPT / 2];
+#pragma unroll
+  for (int e = 0; e < kPT / 2; ++e) t8[e] = fmax_nan(x[2 * e], x[2 * e + 1]);
+#pragma unroll
+  for (int w = kPT / 4; w >= 1; w >>= 1)
+#pragma unroll
+    for (int e = 0; e < w; ++e) t8[e] = fmax_nan(t8[e], t8[e + w]);
+  m = t8[0];
   return m;
 }
 
@@ -484,7 +496,10 @@ __global__ void __launch_bounds__(kNT, 2) stage1_kernel(const Params P) {
   __syncthreads();
 
   long long g = g0;
-  int kst = 0;  // stages consumed by this CTA: slot kst % NS, phase (kst / NS) & 1
+  int kst = 0;           // stages consumed by this CTA
+  int slot = 0;          // kst % NS
+  uint32_t phase = 0u;   // (kst / NS) & 1
+  int c3 = 0;            // kst % 3: this stage's append counter
   int buf = 0;
   bool dead = false;
   while (g < g1 && !dead) {
@@ -557,40 +572,59 @@ __global__ void __launch_bounds__(kNT, 2) stage1_kernel(const Params P) {
           finfo[i] = hval[q];
         }
       __syncthreads();
+      // their exact processed values, read straight from HBM (all loads first),
+      // are the segment's first candidates
+      const int nfl = sm.nf;
+      float raw[kHashMax / kNT];
+      uint32_t mw[kHashMax / kNT];
+#pragma unroll
+      for (int k = 0; k < kHashMax / kNT; ++k) {
+        const int i = tid + k * kNT;
+        raw[k] = 0.0f;
+        mw[k] = 0xFFFFFFFFu;
+        if (i < nfl) {
+          const int tok = ftok[i];
+          raw[k] = load_scalar(P.logits, P.logits_bf16, (int64_t)pos * P.ld + tok);
+          if (mask_on) mw[k] = __ldg(P.bitmask + (size_t)pos * P.mask_words + (tok >> 5));
+        }
+      }
+      bool nan_l = false;
+#pragma unroll
+      for (int k = 0; k < kHashMax / kNT; ++k) {
+        const int i = tid + k * kNT;
+        if (i < nfl) {
+          const int tok = ftok[i];
+          const uint32_t info = finfo[i];
+          float v = raw[k];
+          if (((mw[k] >> (tok & 31)) & 1u) == 0u) v = -INFINITY;
+          v = apply_penalty_bias(v, info & 0x7FFFFFFFu, (info >> 31) != 0u, tok, rc, bl);
+          v = __fmul_rn(v, rc.rT);
+          nan_l |= v != v;
+          cand[i] = pack(v != v ? kKeyNegInf : f2key(v), (uint32_t)tok);
+        }
+      }
+      if (nan_l) sm.nan_flag = 1;
+      __syncthreads();
     }
     const int nf = hashed ? sm.nf : 0;
 
     unsigned long long cutp = 0ull;  // packed cut (0: everything)
-    int n = 0;                       // buffer entries (uniform; read between barriers)
+    int n = nf;                      // buffer entries (uniform; read between barriers)
     float lM = -INFINITY, lS = 0.0f; // this thread's running (max, sum exp) for the normaliser
     bool first = true;
 
     for (; g < ge; ++g, ++kst, first = false) {
-      const int slot = kst % NS;
       const unsigned char* ring = ring0 + (size_t)slot * BN * ESZ;
       const int t0 = (int)(g - gs) * BN;
       const int nt = min(BN, V - t0);
       const bool full = nt == BN;
       const uint32_t* msl = nullptr;
       if (mask_on) msl = mask_tma ? mask0 + (size_t)slot * (BN / 32) : P.bitmask + (size_t)pos * P.mask_words + (t0 >> 5);
-      int* acnt = &sm.cnt[kst % 3];
+      int* acnt = &sm.cnt[c3];
       // the next stage's counter was last read after the barrier two stages back
-      if (tid == 0) sm.cnt[(kst + 1) % 3] = 0;
+      if (tid == 0) sm.cnt[c3 == 2 ? 0 : c3 + 1] = 0;
       // a copy that never lands is noticed by all threads after the stage barrier
-      if (!mbar_wait(&sm.mbar[slot], (uint32_t)((kst / NS) & 1))) sm.dead = 1;
-
-      StageCtx sc;
-      sc.ring = ring;
-      sc.msl = msl;
-      sc.bl = bl;
-      sc.hkey = hkey;
-      sc.hval = hval;
-      sc.aux = aux;
-      sc.rc = rc;
-      sc.t0 = t0;
-      sc.nt = nt;
-      sc.hashed = hashed;
-      sc.staged = staged;
+      if (!mbar_wait(&sm.mbar[slot], phase)) sm.dead = 1;
 
       if (rc.valid) {
         // per-stage count table (long histories, normaliser positions)
@@ -648,7 +682,10 @@ __global__ void __launch_bounds__(kNT, 2) stage1_kernel(const Params P) {
                 const bool isn = xv != xv;
                 nan_seen |= isn;
                 const unsigned long long pk = pack(isn ? kKeyNegInf : f2key(xv), (uint32_t)(t0 + li));
-                if (pk >= cutp && !(aux_on && flag_info(sc, li) != 0u)) append(pk);
+                bool fl = false;
+                if (hashed) fl = hash_find(hkey, t0 + li) >= 0;
+                else if (staged) fl = aux[li] != 0u;
+                if (pk >= cutp && !fl) append(pk);
               }
             }
             if (lse_on) {
@@ -695,6 +732,12 @@ __global__ void __launch_bounds__(kNT, 2) stage1_kernel(const Params P) {
 
         // ---- flagged tokens of this stage, with their exact values
         auto flagged = [&](int li, uint32_t info) {
+          StageCtx sc;
+          sc.ring = ring;
+          sc.msl = msl;
+          sc.bl = bl;
+          sc.rc = rc;
+          sc.t0 = t0;
           const float v = value_with<BF16>(sc, li, info);
           const bool isn = v != v;
           nan_seen |= isn;
@@ -702,12 +745,7 @@ __global__ void __launch_bounds__(kNT, 2) stage1_kernel(const Params P) {
           const unsigned long long pk = pack(isn ? kKeyNegInf : f2key(v), (uint32_t)(t0 + li));
           if (pk >= cutp) append(pk);
         };
-        if (hashed) {
-          for (int i = tid; i < nf; i += kNT) {
-            const int li = ftok[i] - t0;
-            if (li >= 0 && li < nt) flagged(li, finfo[i]);
-          }
-        } else if (staged) {
+        if (staged) {
           const uint4* a4 = reinterpret_cast<const uint4*>(aux);
           for (int w = tid; w < BN / 8; w += kNT) {
             const uint4 a = a4[w];
@@ -732,13 +770,25 @@ __global__ void __launch_bounds__(kNT, 2) stage1_kernel(const Params P) {
 
       // ---- fallback: the buffer overflowed, or the first stage's cut certified too few
       const int need_s = min(kK, nt);
-      if (rc.valid && (n_end > kCap || (first && n_end < need_s))) {
+      if (rc.valid && (n_end > kCap || (first && n_end - n < need_s))) {
         __syncthreads();  // every thread has read the counter
         if (tid == 0) {
           *acnt = 0;  // roll this stage's appends back
           atomicAdd(P.ws.diag + 0, 1u);
         }
         __syncthreads();
+        StageCtx sc;
+        sc.ring = ring;
+        sc.msl = msl;
+        sc.bl = bl;
+        sc.hkey = hkey;
+        sc.hval = hval;
+        sc.aux = aux;
+        sc.rc = rc;
+        sc.t0 = t0;
+        sc.nt = nt;
+        sc.hashed = hashed;
+        sc.staged = staged;
         stage_exact<BF16>(sc, sm, acnt, n, cand, need_s, BN / kNT);
         const int added = min(*acnt, need_s);  // need_s unless the keys disagreed between passes
         unsigned long long mn = ~0ull;
@@ -760,6 +810,11 @@ __global__ void __launch_bounds__(kNT, 2) stage1_kernel(const Params P) {
         n_end = kK;
       }
       n = n_end;
+      if (++slot == NS) {
+        slot = 0;
+        phase ^= 1u;
+      }
+      c3 = c3 == 2 ? 0 : c3 + 1;
     }
     if (dead) break;
 
