@@ -5,19 +5,27 @@
 // One work item per target position (persistent CTAs of 256 threads):
 //  1. merge: each of the position's segments (1..Z_v runs of tiles, one per
 //     stage-1 CTA) left its top-128 packed candidates in the staging buffer.
-//     tau2 = the largest "smallest kept candidate" of a full list certifies
-//     128 candidates, so only packed values >= tau2 enter
-//     shared memory, and a histogram select picks the exact top-128, which a
-//     bitonic network then sorts (processed logit descending, token ascending).
-//  2. epilogue (dl-note Combination): fp64 softmax over the candidates,
-//     top-k / top-p / logit-space min-p cut (shortest prefix), renormalised
-//     kept probabilities; Gumbel-max token in fp32 with Philox noise keyed by
-//     (seed, row, position, token), or the first candidate for greedy rows.
+//     One segment is the answer already; otherwise tau2 = the largest
+//     "smallest kept candidate" of a full list certifies 128 candidates, only
+//     packed values >= tau2 enter shared memory, and a histogram select picks
+//     the exact top-128.  The 128 are ordered (processed logit descending,
+//     token ascending) by ranking: a candidate's place is the number of
+//     candidates above it.
+//  2. epilogue (dl-note Combination): the fp64 softmax weights
+//     w_t = exp(l_t - l_0), one candidate per thread of four warps; then one
+//     warp holding four consecutive candidates per lane: top-k / top-p
+//     (mass before t below top_p) / min-p (l_t - l_0 >= ln min_p, i.e.
+//     w_t >= min_p) cut (shortest prefix), renormalised kept probabilities;
+//     Gumbel-max token in fp32 with Philox noise keyed by (seed, row,
+//     position, token), or the first candidate for greedy rows.
 //  3. verification positions: accept the draft d iff p(d) > 0 and
 //     fp32(u q(d)) <= p(d); on rejection draw from norm(max(0, p - q)) over
 //     the kept set (truncated rows) or queue a pass over the vocabulary
 //     (untruncated rows).  The last position of a row to finish walks the
 //     row: accepted prefix, then the resampled or bonus token.
+// The position's global reads are issued together at its start (row lookup
+// by a 32-way search in one warp while the other warps fetch the lists), so
+// a position costs a few memory round trips and a handful of barriers.
 #include "ss_common.cuh"
 
 namespace ss {
@@ -26,59 +34,61 @@ namespace {
 
 struct S2Smem {
   SelectSmem sel;
-  unsigned long long top[kK];
+  unsigned long long top[kK];  // the selected candidates (unordered)
+  unsigned long long srt[kK];  // the same, ordered
+  double w[kK];                // exp(l_t - l_0) of the ordered candidates (stochastic rows)
   unsigned long long slots[kNT / 32];
-  int r, j, gamma, cnt, out_cnt, last;
+  double lse;
+  int r, j, gamma, c0, cnt, out_cnt, last, token, accept;
   uint32_t status;
-  int d_found;
-  float d_l;
-  double pd, lse, red[kNT / 32];
 };
 
-// Exclusive prefix sum of v over threads 0..kNT-1 in fp64.
-__device__ __forceinline__ double block_exclusive_scan_d(double v, double* scratch) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  double incl = v;
-#pragma unroll
-  for (int d = 1; d < 32; d <<= 1) {
-    const double o = __shfl_up_sync(0xffffffffu, incl, d);
-    if (lane >= d) incl += o;
+// Row of target position pos (the largest r with cu[r] + r <= pos) by one
+// warp: 32-way search rounds over the row offsets.  Every lane gets r.
+__device__ __forceinline__ int warp_find_row(const int32_t* cu, int B, int pos, int lane) {
+  int lo = 0, hi = B - 1;  // r in [lo, hi]; offset(lo) <= pos throughout
+  while (hi > lo) {
+    const int span = hi - lo + 1;
+    const int step = (span + 31) / 32;
+    const int idx = lo + lane * step;
+    const bool ok = idx <= hi && __ldg(cu + idx) + idx <= pos;
+    const uint32_t b = __ballot_sync(0xffffffffu, ok);
+    const int k = 31 - __clz((int)b);  // the last probe at or below pos (probe 0 always is)
+    lo = lo + k * step;
+    hi = min(hi, lo + step - 1);
   }
-  if (lane == 31) scratch[warp] = incl;
-  __syncthreads();
-  double add = 0.0;
-  for (int w = 0; w < warp; ++w) add += scratch[w];
-  __syncthreads();
-  return add + incl - v;
+  return lo;
 }
 
 // Processed logit of one token at one position (the same fp32 steps as the
-// stage-1 prelude), for a draft token outside the candidate list.  All
-// threads call.
-__device__ float prelude_single(const Params& P, const RowCtx& rc, int pos, int r, int j, int tok,
-                                S2Smem& sm) {
+// stage-1 prelude), for a draft token outside the candidate list.  One warp.
+__device__ float prelude_single_warp(const Params& P, const RowCtx& rc, int pos, int r, int c0, int jn, int tok,
+                                     int lane) {
   float x = load_scalar(P.logits, P.logits_bf16, (int64_t)pos * P.ld + tok);
   int cnt = 0;
   if ((rc.flags & SS_PENALTY) && P.history) {
     const int32_t* hrow = P.history + (size_t)r * P.hist_stride;
-    for (int h = threadIdx.x; h < rc.hist_len; h += kNT) cnt += (__ldg(hrow + h) == tok) ? 1 : 0;
-    if (P.cu_draft) {
-      const int base = __ldg(P.cu_draft + r);
-      const int jn = min(j, __ldg(P.cu_draft + r + 1) - base);
-      for (int s = threadIdx.x; s < jn; s += kNT) cnt += (__ldg(P.draft_ids + base + s) == tok) ? 1 : 0;
-    }
+    for (int h = lane; h < rc.hist_len; h += 32) cnt += (__ldg(hrow + h) == tok) ? 1 : 0;
+    if (P.cu_draft)
+      for (int s = lane; s < jn; s += 32) cnt += (__ldg(P.draft_ids + c0 + s) == tok) ? 1 : 0;
   }
-  int total;
-  block_inclusive_scan(cnt, sm.sel.scan, &total);
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, d);
   if ((rc.flags & SS_MASK) && P.bitmask) {
     const uint32_t w = __ldg(P.bitmask + (size_t)pos * P.mask_words + (tok >> 5));
     if (((w >> (tok & 31)) & 1u) == 0u) x = -INFINITY;
   }
   const ss_bias_entry* brow = (rc.flags & SS_BIAS) && P.bias ? P.bias + (size_t)r * P.bias_stride : nullptr;
-  x = apply_penalty_bias(x, (uint32_t)total, brow != nullptr, tok, rc, brow);
+  x = apply_penalty_bias(x, (uint32_t)cnt, brow != nullptr, tok, rc, brow);
   if (rc.stoch) x = __fmul_rn(x, rc.rT);
   if (x != x) x = -INFINITY;
   return x;
+}
+
+__device__ __forceinline__ int warp_sum_i(int v) {
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) v += __shfl_xor_sync(0xffffffffu, v, d);
+  return v;
 }
 
 // Position results written by other CTAs of this kernel: read past L1.
@@ -100,44 +110,53 @@ __global__ void __launch_bounds__(kNT) stage2_kernel(const Params P, int verify)
   unsigned long long* cand = reinterpret_cast<unsigned long long*>(smem_raw);
   unsigned long long* tmp = cand + cap;
   S2Smem& sm = *reinterpret_cast<S2Smem*>(tmp + cap);
-  const int tid = threadIdx.x, lane = tid & 31;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int npos = num_positions(P);
   const int V = P.V, Z = P.Z;
+  const int need = min(kK, V);
+  const long long T = (long long)npos * Z, G = seg_grid(P, T);
 
   for (int pos = blockIdx.x; pos < npos; pos += gridDim.x) {
+    // ---- the position's reads: row lookup (warp 0) beside the lists (all);
+    // every read of the previous position's shared state ended at its last barrier
     if (tid == 0) {
-      int r = pos, j = 0, g = 0;
-      if (P.cu_draft) {
-        r = find_row(P.cu_draft, P.B, pos);
-        const int c0 = __ldg(P.cu_draft + r);
-        j = pos - c0 - r;
-        g = __ldg(P.cu_draft + r + 1) - c0;
-      }
-      sm.r = r;
-      sm.j = j;
-      sm.gamma = g;
       sm.cnt = 0;
       sm.out_cnt = 0;
       sm.status = 0u;
-      sm.d_found = 0;
-      sm.pd = 0.0;
       sm.last = 0;
+      sm.token = -1;
+      sm.accept = 0;
+      sm.lse = 0.0;
     }
+    const int nseg = seg_cta((long long)pos * Z + Z - 1, T, G) - seg_cta((long long)pos * Z, T, G) + 1;
+    const size_t tbase = (size_t)pos * Z;
+    if (warp == 0) {
+      int r = pos, c0 = 0, c1 = 0;
+      if (P.cu_draft) {
+        r = warp_find_row(P.cu_draft, P.B, pos, lane);
+        c0 = __ldg(P.cu_draft + r);
+        c1 = __ldg(P.cu_draft + r + 1);
+      }
+      if (lane == 0) {
+        sm.r = r;
+        sm.c0 = c0;
+        sm.j = P.cu_draft ? pos - c0 - r : 0;
+        sm.gamma = P.cu_draft ? c1 - c0 : 0;
+      }
+    }
+    uint32_t tst = 0u;
+    for (int t = tid; t < nseg; t += kNT) tst |= P.ws.tile_status[tbase + t];
+    const unsigned long long* stg = P.ws.staging + tbase * kK;
+    for (int i = tid; i < nseg * kK; i += kNT) tmp[i] = stg[i];
     __syncthreads();
-    const int r = sm.r, j = sm.j, gamma = sm.gamma;
+    if (tst) atomicOr(&sm.status, tst);
+    const int r = sm.r, j = sm.j, gamma = sm.gamma, c0 = sm.c0;
     const RowCtx rc = make_row(P.rows[r], P.hist_stride, P.bias_stride);
     const uint32_t position = rc.position + (uint32_t)j;
-    // the position's segment lists (the stage-1 split of the npos * Z stages)
-    const long long T = (long long)npos * Z, G = seg_grid(P, T);
-    const int nseg = seg_cta((long long)pos * Z + Z - 1, T, G) - seg_cta((long long)pos * Z, T, G) + 1;
     const uint64_t seed = P.seeds[r];
     const bool is_draft = verify && j >= 0 && j < gamma;
     int32_t* cid = P.out.cand_ids ? P.out.cand_ids + (size_t)pos * kK : nullptr;
     float* cpr = P.out.cand_probs ? P.out.cand_probs + (size_t)pos * kK : nullptr;
-
-    int32_t token = -1;      // sampled / bonus token (or resampled token on rejection)
-    int accept = 0;
-    double lse = 0.0;
 
     if (!rc.valid) {
       if (tid < kK) {
@@ -159,215 +178,289 @@ __global__ void __launch_bounds__(kNT) stage2_kernel(const Params P, int verify)
         for (int e = tid; e < rc.n_bias; e += kNT)
           if (P.bias[(size_t)r * P.bias_stride + e].token >= V) atomicOr(&sm.status, (uint32_t)SS_ST_BAD_BIAS);
       }
-      // ---- 1. merge the tiles' candidates
-      // Load the Z_v * 128 packed candidates; a tile whose 128 slots are all
-      // real certifies 128 candidates >= its smallest one, so tau2 = the
-      // largest such minimum bounds the position's top-128 from below.
-      const size_t tbase = (size_t)pos * Z;
-      uint32_t tst = 0u;
-      for (int t = tid; t < nseg; t += kNT) tst |= P.ws.tile_status[tbase + t];
-      if (tst) atomicOr(&sm.status, tst);
-      const unsigned long long* stg = P.ws.staging + tbase * kK;
-      for (int i = tid; i < nseg * kK; i += kNT) tmp[i] = stg[i];
-      __syncthreads();
-      unsigned long long tm = 0ull;
-      for (int t = tid >> 5; t < nseg; t += kNT / 32) {
-        unsigned long long mn = ~0ull;
+      // ---- 1. merge the segments' candidates
+      if (nseg == 1) {
+        // one segment: its list is the position's top-min(128, V) already
+        if (tid < kK) sm.top[tid] = tid < need ? tmp[tid] : 0ull;
+      } else {
+        unsigned long long tm = 0ull;
+        for (int t = warp; t < nseg; t += kNT / 32) {
+          unsigned long long mn = ~0ull;
 #pragma unroll
-        for (int q = 0; q < kK / 32; ++q) {
-          const unsigned long long c = tmp[t * kK + q * 32 + lane];
-          mn = c < mn ? c : mn;   // an empty slot (0) makes the tile certify nothing
+          for (int q = 0; q < kK / 32; ++q) {
+            const unsigned long long c = tmp[t * kK + q * 32 + lane];
+            mn = c < mn ? c : mn;  // an empty slot (0) makes the list certify nothing
+          }
+          mn = warp_min_u64(mn);
+          tm = mn > tm ? mn : tm;
         }
-        mn = warp_min_u64(mn);
-        tm = mn > tm ? mn : tm;
-      }
-      const unsigned long long tau2 = block_max_u64(tm, sm.slots);
-      unsigned long long lmin = ~0ull, lmax = 0ull;
-      for (int i = tid; i < nseg * kK; i += kNT) {
-        const unsigned long long c = tmp[i];
-        if (c != 0ull && c >= tau2) {
-          cand[atomicAdd(&sm.cnt, 1)] = c;
-          lmin = c < lmin ? c : lmin;
-          lmax = c > lmax ? c : lmax;
+        const unsigned long long tau2 = block_max_u64(tm, sm.slots);
+        unsigned long long lmin = ~0ull, lmax = 0ull;
+        for (int i = tid; i < nseg * kK; i += kNT) {
+          const unsigned long long c = tmp[i];
+          if (c != 0ull && c >= tau2) {
+            cand[atomicAdd(&sm.cnt, 1)] = c;
+            lmin = c < lmin ? c : lmin;
+            lmax = c > lmax ? c : lmax;
+          }
         }
+        const unsigned long long lo = block_min_u64(lmin, sm.slots);
+        const unsigned long long hi = block_max_u64(lmax, sm.slots);
+        const int n = sm.cnt;
+        block_select(cand, tmp, n, need, lo, hi, sm.sel, [&](unsigned long long c) {
+          const int s = atomicAdd(&sm.out_cnt, 1);
+          if (s < kK) sm.top[s] = c;
+        });
+        // slots the select did not fill (only if its count invariant broke) stay empty
+        if (tid < kK && tid >= min(sm.out_cnt, need)) sm.top[tid] = 0ull;
       }
-      const unsigned long long lo = block_min_u64(lmin, sm.slots);
-      const unsigned long long hi = block_max_u64(lmax, sm.slots);
-      const int n = sm.cnt;
-      const int need = min(kK, V);
-      block_select(cand, tmp, n, need, lo, hi, sm.sel,
-                   [&](unsigned long long c) {
-                     const int s = atomicAdd(&sm.out_cnt, 1);
-                     if (s < kK) sm.top[s] = c;
-                   });
-      // slots the select did not fill (only if its count invariant broke) stay empty
-      if (tid < kK && tid >= min(sm.out_cnt, need)) sm.top[tid] = 0ull;
       __syncthreads();
-      // bitonic sort of the 128 candidates, descending
-      for (int k = 2; k <= kK; k <<= 1) {
-        for (int d = k >> 1; d > 0; d >>= 1) {
-          if (tid < kK) {
-            const int p = tid ^ d;
-            if (p > tid) {
-              const unsigned long long a = sm.top[tid], b = sm.top[p];
-              const bool desc = (tid & k) == 0;
-              if ((a < b) == desc) {
-                sm.top[tid] = b;
-                sm.top[p] = a;
+      // order: a candidate's place is the number of candidates above it
+      // (distinct values; empty slots (0) rank below every candidate)
+      const unsigned long long v = tid < kK ? sm.top[tid] : 0ull;
+      const int nz = __syncthreads_count(v != 0ull);
+      if (v != 0ull) {
+        int rank = 0;
+#pragma unroll 8
+        for (int u = 0; u < kK; ++u) rank += sm.top[u] > v ? 1 : 0;
+        sm.srt[rank] = v;
+      }
+      if (tid < kK && tid >= nz) sm.srt[tid] = 0ull;
+      __syncthreads();
+      // softmax weights, one candidate per thread (the fp64 exp spread over
+      // four warps): w_t = exp(l_t - l_0) for finite l_t; unused for point masses
+      if (tid < kK) {
+        const unsigned long long c = sm.srt[tid];
+        const float lt = (tid < need && c != 0ull) ? key2f(pk_key(c)) : -INFINITY;
+        const float lz = key2f(pk_key(sm.srt[0]));
+        sm.w[tid] = (rc.stoch && lt > -INFINITY && lz < INFINITY) ? exp((double)lt - (double)lz) : 0.0;
+      }
+      __syncthreads();
+
+      if (warp == 0) {
+        // ---- 2. epilogue: lane L holds the ordered candidates 4L .. 4L + 3
+        unsigned long long cv[4];
+        bool real[4], fin[4];
+        int32_t tok[4];
+        float l[4];
+        int nfin = 0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int t = 4 * lane + k;
+          cv[k] = sm.srt[t];
+          real[k] = t < need && cv[k] != 0ull;
+          tok[k] = pk_tok(cv[k]);
+          l[k] = real[k] ? key2f(pk_key(cv[k])) : -INFINITY;
+          fin[k] = real[k] && l[k] > -INFINITY;
+          nfin += fin[k] ? 1 : 0;
+        }
+        const float l0 = key2f(pk_key(sm.srt[0]));
+        const int32_t tok0 = pk_tok(sm.srt[0]);
+        const int n_f = warp_sum_i(nfin);
+        const bool no_finite = n_f == 0;
+        const bool pos_inf = !no_finite && l0 == INFINITY;
+        const bool point = no_finite || pos_inf || !rc.stoch;
+        int nk = 0;
+        double w[4] = {0.0, 0.0, 0.0, 0.0};
+        double zk = 1.0;
+        if (no_finite) {
+          nk = 0;
+        } else if (point) {
+          nk = 1;
+        } else {
+          double ls = 0.0;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            w[k] = sm.w[4 * lane + k];
+            ls += w[k];
+          }
+          const double Zall = warp_sum_d(ls);
+          int n2 = min(need, n_f);
+          if ((rc.flags & SS_TOPK) && rc.top_k > 0) n2 = min(n2, rc.top_k);
+          if ((rc.flags & SS_TOPP) && rc.top_p < 1.0f) {
+            // t is kept iff the mass before it, sum_{u<t} w_u / Z, is below top_p:
+            // the exclusive prefix of w in candidate order against top_p * Z
+            double e[4], run = 0.0;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              e[k] = run;
+              run += (4 * lane + k < need) ? w[k] : 0.0;
+            }
+            double incl = run;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+              const double o = __shfl_up_sync(0xffffffffu, incl, d);
+              if (lane >= d) incl += o;
+            }
+            const double base = incl - run;
+            const double lim = (double)rc.top_p * Zall;
+            int c = 0;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) c += (4 * lane + k < need && base + e[k] < lim) ? 1 : 0;
+            n2 = min(n2, warp_sum_i(c));
+          }
+          if ((rc.flags & SS_MINP) && rc.min_p > 0.0f) {
+            // l_t - l_0 >= ln(min_p)  <=>  w_t = exp(l_t - l_0) >= min_p
+            int c = 0;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) c += (4 * lane + k < need && w[k] >= (double)rc.min_p) ? 1 : 0;
+            n2 = min(n2, warp_sum_i(c));
+          }
+          nk = max(1, n2);
+          double kz = 0.0;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) kz += (4 * lane + k < nk) ? w[k] : 0.0;
+          zk = warp_sum_d(kz);
+        }
+        const double izk = 1.0 / zk;
+        // candidate outputs
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int t = 4 * lane + k;
+          if (cid) cid[t] = real[k] ? tok[k] : -1;
+          if (cpr) {
+            float pr = 0.0f;
+            if (t < nk) pr = point ? (t == 0 ? 1.0f : 0.0f) : (float)(w[k] * izk);
+            cpr[t] = pr;
+          }
+        }
+        uint32_t st = 0u;
+        if (no_finite) st |= SS_ST_NO_FINITE;
+        else if (pos_inf) st |= SS_ST_POS_INF;
+
+        // ---- 3. token of this position (sample / bonus)
+        int32_t token = -1;
+        int accept = 0;
+        double lse = 0.0;
+        if (!is_draft) {
+          if (no_finite) {
+            token = -1;
+          } else if (point) {
+            token = tok0;
+          } else {
+            unsigned long long sc = 0ull;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              if (4 * lane + k < nk) {
+                const float g = gumbel_of(philox_uniform(seed, (uint32_t)tok[k], position, (uint32_t)r, 0u));
+                const unsigned long long s = pack(f2key(__fadd_rn(l[k], g)), (uint32_t)tok[k]);
+                sc = s > sc ? s : sc;
               }
             }
+            token = pk_tok(warp_max_u64(sc));
           }
-          __syncthreads();
-        }
-      }
-
-      // ---- 2. epilogue over the candidates (thread t < 128 holds candidate t)
-      const int t = tid;
-      const unsigned long long c = t < kK ? sm.top[t] : 0ull;
-      const bool real = t < need && c != 0ull;
-      const int32_t tok = pk_tok(c);
-      const float l = real ? key2f(pk_key(c)) : -INFINITY;
-      const float l0 = key2f(pk_key(sm.top[0]));
-      const int32_t tok0 = pk_tok(sm.top[0]);
-      const bool finite = real && l > -INFINITY;
-      const int n_f = __syncthreads_count(finite);
-      const bool no_finite = n_f == 0;
-      const bool pos_inf = !no_finite && l0 == INFINITY;
-      const bool point = no_finite || pos_inf || !rc.stoch;
-      int nk = 0;
-      double w = 0.0, zk = 1.0;
-      if (no_finite) {
-        nk = 0;
-      } else if (point) {
-        nk = 1;
-      } else {
-        w = finite ? exp((double)l - (double)l0) : 0.0;
-        const double Zall = block_sum_d(w, sm.red);
-        int n2 = min(need, n_f);
-        if ((rc.flags & SS_TOPK) && rc.top_k > 0) n2 = min(n2, rc.top_k);
-        if ((rc.flags & SS_TOPP) && rc.top_p < 1.0f) {
-          const double ex = block_exclusive_scan_d(t < need ? w / Zall : 0.0, sm.red);
-          const int np = __syncthreads_count(t < need && ex < (double)rc.top_p);
-          n2 = min(n2, np);
-        }
-        if ((rc.flags & SS_MINP) && rc.min_p > 0.0f) {
-          const double thr = log((double)rc.min_p);
-          const int nm = __syncthreads_count(t < need && ((double)l - (double)l0) >= thr);
-          n2 = min(n2, nm);
-        }
-        nk = max(1, n2);
-        zk = block_sum_d(t < nk ? w : 0.0, sm.red);
-      }
-      // candidate outputs
-      if (t < kK) {
-        if (cid) cid[t] = real ? tok : -1;
-        if (cpr) {
-          float pr = 0.0f;
-          if (t < nk) pr = point ? (t == 0 ? 1.0f : 0.0f) : (float)(w / zk);
-          cpr[t] = pr;
-        }
-      }
-      if (tid == 0 && P.out.num_kept) P.out.num_kept[pos] = nk;
-      if (no_finite) {
-        if (tid == 0) atomicOr(&sm.status, (uint32_t)SS_ST_NO_FINITE);
-      } else if (pos_inf && tid == 0) {
-        atomicOr(&sm.status, (uint32_t)SS_ST_POS_INF);
-      }
-
-      // ---- 3. token of this position (sample / bonus)
-      if (!is_draft) {
-        if (no_finite) {
-          token = -1;
-        } else if (point) {
-          token = tok0;
         } else {
-          unsigned long long sc = 0ull;
-          if (t < nk) {
-            const float g = gumbel_of(philox_uniform(seed, (uint32_t)tok, position, (uint32_t)r, 0u));
-            sc = pack(f2key(__fadd_rn(l, g)), (uint32_t)tok);
-          }
-          token = pk_tok(block_max_u64(sc, sm.slots));
-        }
-      } else {
-        // ---- 4. verification of draft j
-        const int32_t d = __ldg(P.draft_ids + __ldg(P.cu_draft + r) + j);
-        const bool d_ok = d >= 0 && d < V;
-        if (!d_ok && tid == 0) atomicOr(&sm.status, (uint32_t)SS_ST_BAD_DRAFT);
-        if (no_finite) {
-          accept = 0;
-          token = -1;
-        } else if (point) {
-          accept = (d_ok && d == tok0) ? 1 : 0;
-          token = tok0;
-        } else {
-          const int64_t qrow = (int64_t)__ldg(P.cu_draft + r) + j;
-          if (rc.trunc) {
-            if (t < nk && tok == d) sm.pd = w / zk;
-            __syncthreads();
+          // ---- 4. verification of draft j
+          const int32_t d = __ldg(P.draft_ids + c0 + j);
+          const bool d_ok = d >= 0 && d < V;
+          if (!d_ok) st |= SS_ST_BAD_DRAFT;
+          if (no_finite) {
+            accept = 0;
+            token = -1;
+          } else if (point) {
+            accept = (d_ok && d == tok0) ? 1 : 0;
+            token = tok0;
           } else {
-            // full-vocabulary softmax: LSE from the tiles' (max, sum exp) partials
-            if (tid == 0) {
+            const int64_t qrow = (int64_t)c0 + j;
+            double pd = 0.0;
+            if (rc.trunc) {
+              double mine = 0.0;
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                if (4 * lane + k < nk && tok[k] == d) mine = w[k] / zk;
+#pragma unroll
+              for (int dd = 16; dd > 0; dd >>= 1) mine = fmax(mine, __shfl_xor_sync(0xffffffffu, mine, dd));
+              pd = mine;
+            } else {
+              // full-vocabulary softmax: LSE from the segments' (max, sum exp) partials
               float M = -INFINITY;
-              for (int tt = 0; tt < nseg; ++tt) M = fmaxf(M, P.ws.tile_lse[(size_t)pos * Z + tt].x);
+              for (int tt = 0; tt < nseg; ++tt) M = fmaxf(M, P.ws.tile_lse[tbase + tt].x);
               double S = 0.0;
               for (int tt = 0; tt < nseg; ++tt) {
-                const float2 ms = P.ws.tile_lse[(size_t)pos * Z + tt];
+                const float2 ms = P.ws.tile_lse[tbase + tt];
                 if (ms.x > -INFINITY) S += (double)ms.y * exp((double)ms.x - (double)M);
               }
-              sm.lse = (double)M + log(S);
-            }
-            if (real && tok == d) {
-              sm.d_found = 1;
-              sm.d_l = l;
-            }
-            __syncthreads();
-            lse = sm.lse;
-            float ld = sm.d_l;
-            if (!sm.d_found && d_ok) ld = prelude_single(P, rc, pos, r, j, d, sm);
-            if (tid == 0 && d_ok) sm.pd = exp((double)ld - lse);
-            __syncthreads();
-          }
-          const double pd = sm.pd;
-          if (d_ok) {
-            const float u = philox_uniform(seed, 0u, position, (uint32_t)r, 1u);
-            const float prod = __fmul_rn(u, load_scalar(P.q, P.q_bf16, qrow * P.ld_q + d));
-            accept = (pd > 0.0 && (double)prod <= pd) ? 1 : 0;
-          }
-          if (!accept) {
-            if (rc.trunc) {
-              // residual norm(max(0, p - q)) over the kept candidates
-              double rr = 0.0;
-              if (t < nk) rr = fmax(0.0, w / zk - (double)load_scalar(P.q, P.q_bf16, qrow * P.ld_q + tok));
-              const int anypos = __syncthreads_or(t < nk && rr > 0.0);
-              unsigned long long sc = 0ull;
-              if (t < nk) {
-                const float g = gumbel_of(philox_uniform(seed, (uint32_t)tok, position, (uint32_t)r, 2u));
-                if (anypos) {
-                  if (rr > 0.0) sc = pack(f2key(__fadd_rn(logf((float)rr), g)), (uint32_t)tok);
-                } else {
-                  sc = pack(f2key(__fadd_rn(l, g)), (uint32_t)tok);
+              lse = (double)M + log(S);
+              // d among the candidates: its logit; else recompute it
+              bool found = false;
+              float dl = 0.0f;
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                if (real[k] && tok[k] == d) {
+                  found = true;
+                  dl = l[k];
                 }
+              const uint32_t fb = __ballot_sync(0xffffffffu, found);
+              if (fb) {
+                dl = __shfl_sync(0xffffffffu, dl, __ffs((int)fb) - 1);
+              } else if (d_ok) {
+                dl = prelude_single_warp(P, rc, pos, r, c0, min(j, gamma), d, lane);
               }
-              token = pk_tok(block_max_u64(sc, sm.slots));
-              if (!anypos && tid == 0) atomicOr(&sm.status, (uint32_t)SS_ST_RESID_EMPTY);
-            } else {
-              token = kPending;  // drawn by the pass over the vocabulary
+              if (d_ok) pd = exp((double)dl - lse);
+            }
+            if (d_ok) {
+              const float u = philox_uniform(seed, 0u, position, (uint32_t)r, 1u);
+              const float prod = __fmul_rn(u, load_scalar(P.q, P.q_bf16, qrow * P.ld_q + d));
+              accept = (pd > 0.0 && (double)prod <= pd) ? 1 : 0;
+            }
+            if (!accept) {
+              if (rc.trunc) {
+                // residual norm(max(0, p - q)) over the kept candidates
+                double rr[4];
+                bool pos_any = false;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                  rr[k] = 0.0;
+                  if (4 * lane + k < nk)
+                    rr[k] = fmax(0.0, w[k] * izk - (double)load_scalar(P.q, P.q_bf16, qrow * P.ld_q + tok[k]));
+                  pos_any |= (4 * lane + k < nk && rr[k] > 0.0);
+                }
+                const bool anypos = __any_sync(0xffffffffu, pos_any);
+                unsigned long long sc = 0ull;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                  if (4 * lane + k < nk) {
+                    const float g = gumbel_of(philox_uniform(seed, (uint32_t)tok[k], position, (uint32_t)r, 2u));
+                    unsigned long long s = 0ull;
+                    if (anypos) {
+                      if (rr[k] > 0.0) s = pack(f2key(__fadd_rn(logf((float)rr[k]), g)), (uint32_t)tok[k]);
+                    } else {
+                      s = pack(f2key(__fadd_rn(l[k], g)), (uint32_t)tok[k]);
+                    }
+                    sc = s > sc ? s : sc;
+                  }
+                }
+                token = pk_tok(warp_max_u64(sc));
+                if (!anypos) st |= SS_ST_RESID_EMPTY;
+              } else {
+                token = kPending;  // drawn by the pass over the vocabulary
+              }
             }
           }
+        }
+        if (lane == 0) {
+          if (P.out.num_kept) P.out.num_kept[pos] = nk;
+          if (st) atomicOr(&sm.status, st);
+          sm.token = token;
+          sm.accept = accept;
+          sm.lse = lse;
         }
       }
     }
     __syncthreads();
     const uint32_t status = sm.status;
+    const int32_t token = rc.valid ? sm.token : -1;
+    const int accept = rc.valid ? sm.accept : 0;
+    const double lse = sm.lse;
 
     // ---- 5. outputs
     if (!verify) {
       if (tid == 0) {
-        P.out.tokens[r] = rc.valid ? token : -1;
+        P.out.tokens[r] = token;
         P.out.row_status[r] = status;
       }
-    } else {
-      if (tid == 0) {
+    } else if (warp == 0) {
+      if (lane == 0) {
         PosResult pr;
         pr.lse = lse;
         pr.token = token;
@@ -379,49 +472,59 @@ __global__ void __launch_bounds__(kNT) stage2_kernel(const Params P, int verify)
         const uint32_t old = atomicAdd(P.ws.row_count + r, 1u);
         sm.last = (old == (uint32_t)gamma) ? 1 : 0;
       }
-      __syncthreads();
-      if (sm.last && tid == 0) {
-        // the row's last position: walk the drafts
+      __syncwarp();
+      if (sm.last) {
+        // the row's last position: walk the drafts (one warp; positions read in parallel)
         __threadfence();
-        const int pos0 = __ldg(P.cu_draft + r) + r;
+        const int pos0 = c0 + r;
         int32_t* tk = P.out.tokens + (size_t)r * P.out.tokens_stride;
         const int stride = P.out.tokens_stride;
         uint32_t st = 0u;
         int n_acc = 0;
         if (!rc.valid) {
-          for (int s = 0; s < stride; ++s) tk[s] = -1;
+          for (int s = lane; s < stride; s += 32) tk[s] = -1;
           st = SS_ST_BAD_PARAM;
         } else {
           int stop = gamma;
-          for (int s = 0; s < gamma; ++s) {
-            const PosResult q = load_pos_result(P.ws.pos + pos0 + s);
-            st |= q.status;
-            if (!q.accept) {
-              stop = s;
-              break;
-            }
+          for (int s0 = 0; s0 < gamma && stop == gamma; s0 += 32) {
+            const int s = s0 + lane;
+            PosResult q;
+            q.status = 0u;
+            q.accept = 1;
+            if (s < gamma) q = load_pos_result(P.ws.pos + pos0 + s);
+            const uint32_t rej = __ballot_sync(0xffffffffu, s < gamma && !q.accept);
+            const int first = rej ? s0 + __ffs((int)rej) - 1 : gamma;
+            // statuses of the drafts up to and including the first rejection
+            uint32_t sv = (s < gamma && s <= first) ? q.status : 0u;
+#pragma unroll
+            for (int d = 16; d > 0; d >>= 1) sv |= __shfl_xor_sync(0xffffffffu, sv, d);
+            st |= sv;
+            stop = first;
           }
-          const int base = __ldg(P.cu_draft + r);
-          for (int s = 0; s < stop && s < stride; ++s) tk[s] = __ldg(P.draft_ids + base + s);
+          for (int s = lane; s < stop && s < stride; s += 32) tk[s] = __ldg(P.draft_ids + c0 + s);
           const PosResult fin = load_pos_result(P.ws.pos + pos0 + stop);
           if (stop == gamma) st |= fin.status;
-          int32_t ft = fin.token;
-          if (ft == kPending) {
-            if (stop < stride) {
-              const uint32_t e = atomicAdd(P.ws.resid_count, 1u);
-              P.ws.resid[e].row = r;
-              P.ws.resid[e].j = stop;
-              P.ws.resid[e].pos = pos0 + stop;
+          if (lane == 0) {
+            int32_t ft = fin.token;
+            if (ft == kPending) {
+              if (stop < stride) {
+                const uint32_t e = atomicAdd(P.ws.resid_count, 1u);
+                P.ws.resid[e].row = r;
+                P.ws.resid[e].j = stop;
+                P.ws.resid[e].pos = pos0 + stop;
+              }
+              ft = -1;  // written by the residual pass
             }
-            ft = -1;  // written by the residual pass
+            if (stop < stride) tk[stop] = ft;
           }
-          if (stop < stride) tk[stop] = ft;
-          for (int s = stop + 1; s < stride; ++s) tk[s] = -1;
+          for (int s = stop + 1 + lane; s < stride; s += 32) tk[s] = -1;
           n_acc = stop;
         }
-        if (P.out.num_accepted) P.out.num_accepted[r] = n_acc;
-        P.out.row_status[r] = st;
-        P.ws.row_count[r] = 0u;
+        if (lane == 0) {
+          if (P.out.num_accepted) P.out.num_accepted[r] = n_acc;
+          P.out.row_status[r] = st;
+          P.ws.row_count[r] = 0u;
+        }
       }
     }
     __syncthreads();
