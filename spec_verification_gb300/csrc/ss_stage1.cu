@@ -40,8 +40,9 @@
 //    values, NaN, penalised maxima) is rolled back and replaced by an exact
 //    radix select of the stage's top-128, after which the cut is raised to
 //    the stage's 128th value.  Both invariants survive every step.
-//  - the segment's NaN status and, for untruncated stochastic verify
-//    positions, (max, sum exp(x - max)) over the segment go beside the list.
+//  - the segment's status (NaN seen; history / bias ids beyond the
+//    vocabulary) and, for untruncated stochastic verify positions,
+//    (max, sum exp(x - max)) over the segment go beside the list.
 #include <type_traits>
 
 #include "ss_common.cuh"
@@ -85,6 +86,8 @@ struct __align__(16) S1Smem {
   float lm[kNT / 32];
   int cnt[3];  // appends of stage k go to cnt[k % 3]
   int dead, nan_flag, nf, out_cnt;
+  uint32_t rowbad;  // SS_ST_BAD_HIST / SS_ST_BAD_BIAS of the segment's row
+  int pad2[3];
 };
 
 struct Layout {
@@ -536,6 +539,7 @@ __global__ void __launch_bounds__(kNT, 2) stage1_kernel(const Params P) {
       sm.cnt[0] = sm.cnt[1] = sm.cnt[2] = 0;
       sm.nan_flag = 0;
       sm.nf = 0;
+      sm.rowbad = 0u;
     }
     if (hashed)
       for (int q = tid; q < kHash; q += kNT) {
@@ -543,6 +547,15 @@ __global__ void __launch_bounds__(kNT, 2) stage1_kernel(const Params P) {
         hval[q] = 0u;
       }
     __syncthreads();
+    // history / bias ids beyond the vocabulary are ignored and reported
+    if (pen_on) {
+      const int32_t* hrow = P.history + (size_t)r * P.hist_stride;
+      for (int h = tid; h < rc.hist_len; h += kNT)
+        if ((h < kPre ? cb.hist[h] : __ldg(hrow + h)) >= V) atomicOr(&sm.rowbad, (uint32_t)SS_ST_BAD_HIST);
+    }
+    if (bias_on)
+      for (int e = tid; e < rc.n_bias; e += kNT)
+        if ((e < kBiasPre ? cb.bias[e].token : brow[e].token) >= V) atomicOr(&sm.rowbad, (uint32_t)SS_ST_BAD_BIAS);
     if (hashed) {
       auto insert = [&](int tok, uint32_t add, uint32_t orv) {
         if (tok < seg_lo || tok >= seg_hi) return;  // also drops padding (< 0) and ids >= V
@@ -829,7 +842,7 @@ __global__ void __launch_bounds__(kNT, 2) stage1_kernel(const Params P) {
         if (q < kK) stg[q] = c;
       });
       for (int q = min(sm.out_cnt, need) + tid; q < kK; q += kNT) stg[q] = 0ull;
-      if (tid == 0) P.ws.tile_status[lslot] = sm.nan_flag ? SS_ST_NAN : 0u;
+      if (tid == 0) P.ws.tile_status[lslot] = (sm.nan_flag ? SS_ST_NAN : 0u) | sm.rowbad;
       if (lse_on) {
         float Mb = lM;
 #pragma unroll

@@ -39,7 +39,8 @@ struct S2Smem {
   double w[kK];                // exp(l_t - l_0) of the ordered candidates (stochastic rows)
   unsigned long long slots[kNT / 32];
   double lse;
-  int r, j, gamma, c0, cnt, out_cnt, last, token, accept;
+  int r, j, gamma, c0, cnt, out_cnt, last, token, accept, d;
+  float qd;
   uint32_t status;
 };
 
@@ -138,10 +139,21 @@ __global__ void __launch_bounds__(kNT) stage2_kernel(const Params P, int verify)
         c1 = __ldg(P.cu_draft + r + 1);
       }
       if (lane == 0) {
+        const int j = P.cu_draft ? pos - c0 - r : 0;
+        const int gamma = P.cu_draft ? c1 - c0 : 0;
         sm.r = r;
         sm.c0 = c0;
-        sm.j = P.cu_draft ? pos - c0 - r : 0;
-        sm.gamma = P.cu_draft ? c1 - c0 : 0;
+        sm.j = j;
+        sm.gamma = gamma;
+        // a draft position's token and q(d), fetched beside the lists
+        int32_t d = -1;
+        float qd = 0.0f;
+        if (verify && j < gamma) {
+          d = __ldg(P.draft_ids + c0 + j);
+          if (d >= 0 && d < V) qd = load_scalar(P.q, P.q_bf16, ((int64_t)c0 + j) * P.ld_q + d);
+        }
+        sm.d = d;
+        sm.qd = qd;
       }
     }
     uint32_t tst = 0u;
@@ -168,16 +180,6 @@ __global__ void __launch_bounds__(kNT) stage2_kernel(const Params P, int verify)
         atomicOr(&sm.status, (uint32_t)SS_ST_BAD_PARAM);
       }
     } else {
-      // ---- row-level input checks (history / bias ids beyond the vocabulary)
-      if ((rc.flags & SS_PENALTY) && P.history) {
-        const int32_t* hrow = P.history + (size_t)r * P.hist_stride;
-        for (int h = tid; h < rc.hist_len; h += kNT)
-          if (__ldg(hrow + h) >= V) atomicOr(&sm.status, (uint32_t)SS_ST_BAD_HIST);
-      }
-      if ((rc.flags & SS_BIAS) && P.bias) {
-        for (int e = tid; e < rc.n_bias; e += kNT)
-          if (P.bias[(size_t)r * P.bias_stride + e].token >= V) atomicOr(&sm.status, (uint32_t)SS_ST_BAD_BIAS);
-      }
       // ---- 1. merge the segments' candidates
       if (nseg == 1) {
         // one segment: its list is the position's top-min(128, V) already
@@ -351,7 +353,7 @@ __global__ void __launch_bounds__(kNT) stage2_kernel(const Params P, int verify)
           }
         } else {
           // ---- 4. verification of draft j
-          const int32_t d = __ldg(P.draft_ids + c0 + j);
+          const int32_t d = sm.d;
           const bool d_ok = d >= 0 && d < V;
           if (!d_ok) st |= SS_ST_BAD_DRAFT;
           if (no_finite) {
@@ -400,7 +402,7 @@ __global__ void __launch_bounds__(kNT) stage2_kernel(const Params P, int verify)
             }
             if (d_ok) {
               const float u = philox_uniform(seed, 0u, position, (uint32_t)r, 1u);
-              const float prod = __fmul_rn(u, load_scalar(P.q, P.q_bf16, qrow * P.ld_q + d));
+              const float prod = __fmul_rn(u, sm.qd);
               accept = (pd > 0.0 && (double)prod <= pd) ? 1 : 0;
             }
             if (!accept) {
