@@ -162,6 +162,23 @@ def dist_setup():
     return world, rank, local
 
 
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """The largest x over the ranks (the slowest rank's time); x itself on one rank."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(world: int, rows: int, steps: int, ms: float) -> float:
+    """Rows per second over all ranks: each rank runs its own copy of the
+    workload (replicas, weak scaling) and the job takes the slowest rank's time."""
+    return world * rows * steps / (ms / 1e3)
+
+
 def num_segments(npos: int, z: int, ctas: int) -> int:
     """Segments of the stage-1 split: the npos * z tiles are cut into
     g = min(ctas, npos * z) contiguous runs (run c starts at c * T // g), and
@@ -302,11 +319,7 @@ def run_ours(args, w, desc):
     st1 = [event_ms(ev[i][0], ev[i][1]) for i in range(G)]
     st2 = [event_ms(ev[i][1], ev[i][2]) for i in range(G)]
     st3 = [event_ms(ev[i][2], ev[i][3]) for i in range(G)]
-    ms_max = ms
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_max = float(t.item())
+    ms_max = max_over_ranks(ms, world, dev)
 
     # end to end: inputs from pinned host memory, tokens back, every step
     e2e = None
@@ -340,12 +353,8 @@ def run_ours(args, w, desc):
                 e2e_step()
             b.record(stream)
         torch.cuda.synchronize(dev)
-        ems = a.elapsed_time(b)
-        if world > 1:
-            t = torch.tensor([ems], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ems = float(t.item())
-        e2e = {"value": world * w.B * E / (ems / 1e3), "unit": "rows/s",
+        ems = max_over_ranks(a.elapsed_time(b), world, dev)
+        e2e = {"value": whole_job_rate(world, w.B, E, ems), "unit": "rows/s",
                "h2d_bytes_per_step": hrun.input_bytes(), "d2h_bytes_per_step": hrun.output_bytes(),
                "steps": E, "ms_per_step": ems / E}
         del hrun
@@ -357,7 +366,7 @@ def run_ours(args, w, desc):
     achieved = alg1 / t1 / 1e9
     traffic = profiled_traffic(args.workload)
     counted = w.counted_bytes(8192)  # the metric's definition: staging of 8192-token tiles
-    value = world * w.B * K / (ms_max / 1e3)
+    value = whole_job_rate(world, w.B, K, ms_max)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
         cpu = cpu_baseline(w, args.workload, args.cpu_seconds)
