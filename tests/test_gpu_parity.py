@@ -130,6 +130,29 @@ def test_bad_params_and_ids():
     check(w)
 
 
+def test_long_history_uses_count_tables():
+    # more history / bias tokens than a segment's hash table lists (512): the
+    # per-stage count tables of stage 1 handle these rows
+    w = W.sample_workload(29, 8, 60000, "f32", H=1500, NB=24)
+    assert int(w.rows["hist_len"].max()) > 512
+    check(w)
+
+
+def test_ascending_rows_overflow_into_exact_fallback():
+    # logits rising along the row: every stage lifts a crowd of elements over
+    # the running cut, the append buffer overflows and the stage is replaced
+    # by its exact top-128
+    # (48 rows x 16 tiles: more tiles than stage-1 CTAs, so segments span
+    # several tiles and the later ones overflow)
+    rng = np.random.default_rng(31)
+    B, V = 48, 131072
+    x = (np.linspace(-6.0, 6.0, V, dtype=np.float32)[None, :]
+         + rng.standard_normal((B, V)).astype(np.float32) * np.float32(1e-3))
+    w = sample_case(x, flags=F.TOPP, top_p=0.9, temperature=[1.0] * B)
+    _, _, d = check(w)
+    assert d.diag()[0] > 0
+
+
 def test_deterministic_repeat():
     w = W.sample_workload(25, 8, 60000, "bf16")
     from spec_verification_gb300.runner import DeviceRun
