@@ -19,6 +19,7 @@ __global__ void residual_kernel(const Params P);
 size_t stage1_smem_bytes(int BN, bool bf16, int nslot);
 int stage1_max_slots();
 size_t stage2_smem_bytes(int Z);
+int stage2_threads();
 size_t residual_smem_bytes(int BN);
 }  // namespace ss
 
@@ -148,7 +149,7 @@ ss_status ss_plan_create(ss_plan** out, int32_t V, int32_t max_rows, int32_t max
   int occ1 = 0, occ2 = 0, occ3 = 0;
   if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ1, p->k1, ss::kNT, p->smem1);
   if (e == cudaSuccess)
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ2, ss::stage2_kernel, ss::kNT, p->smem2);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ2, ss::stage2_kernel, ss::stage2_threads(), p->smem2);
   if (e == cudaSuccess)
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ3, ss::residual_kernel, ss::kNT, p->smem3);
   if (e != cudaSuccess) {
@@ -256,7 +257,7 @@ ss_status launch(const ss_plan* pl, const ss::Params& P, cudaStream_t st, bool v
   rec(0);
   ss::stage1_launch(pl->ldt == SS_BF16, pl->grid1, pl->smem1, st, P);
   rec(1);
-  ss::stage2_kernel<<<pl->grid2, ss::kNT, pl->smem2, st>>>(P, verify ? 1 : 0);
+  ss::stage2_kernel<<<pl->grid2, ss::stage2_threads(), pl->smem2, st>>>(P, verify ? 1 : 0);
   rec(2);
   if (verify) ss::residual_kernel<<<pl->grid3, ss::kNT, pl->smem3, st>>>(P);
   rec(3);

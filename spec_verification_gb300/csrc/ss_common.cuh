@@ -298,25 +298,27 @@ __device__ __forceinline__ unsigned long long warp_min_u64(unsigned long long v)
 }
 
 // Block-wide max / min of a 64-bit value through per-warp slots (no 64-bit
-// shared-memory atomics, which serialise under contention).  All threads
-// call; `slots` holds kNT/32 values; every thread gets the result.
+// shared-memory atomics, which serialise under contention).  All NT threads
+// of the block call; `slots` holds NT/32 values; every thread gets the result.
+template <int NT = kNT>
 __device__ __forceinline__ unsigned long long block_max_u64(unsigned long long v, unsigned long long* slots) {
   v = warp_max_u64(v);
   if ((threadIdx.x & 31) == 0) slots[threadIdx.x >> 5] = v;
   __syncthreads();
   unsigned long long r = slots[0];
 #pragma unroll
-  for (int w = 1; w < kNT / 32; ++w) r = slots[w] > r ? slots[w] : r;
+  for (int w = 1; w < NT / 32; ++w) r = slots[w] > r ? slots[w] : r;
   __syncthreads();
   return r;
 }
+template <int NT = kNT>
 __device__ __forceinline__ unsigned long long block_min_u64(unsigned long long v, unsigned long long* slots) {
   v = warp_min_u64(v);
   if ((threadIdx.x & 31) == 0) slots[threadIdx.x >> 5] = v;
   __syncthreads();
   unsigned long long r = slots[0];
 #pragma unroll
-  for (int w = 1; w < kNT / 32; ++w) r = slots[w] < r ? slots[w] : r;
+  for (int w = 1; w < NT / 32; ++w) r = slots[w] < r ? slots[w] : r;
   __syncthreads();
   return r;
 }
@@ -383,11 +385,11 @@ __device__ __forceinline__ uint32_t bin_of(unsigned long long c, unsigned long l
 // remaining value range; a boundary bin of at most 32 values is ranked by one
 // warp.  Selected values go to emit(c) (unordered).  tmp has room for n
 // values.  All threads call with uniform arguments.
-template <class Emit>
+template <int NT = kNT, class Emit>
 __device__ void block_select(unsigned long long* cand, unsigned long long* tmp, int n, int need,
                              unsigned long long lo, unsigned long long hi, SelectSmem& S, Emit emit) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (tid < 256) S.hist[tid] = 0u;
+  for (int q = tid; q < 256; q += NT) S.hist[q] = 0u;
   if (tid == 0) {
     S.tcnt[0] = 0;
     S.tcnt[1] = 0;
@@ -396,7 +398,7 @@ __device__ void block_select(unsigned long long* cand, unsigned long long* tmp, 
   for (int iter = 0; iter < 16; ++iter) {
     if (need <= 0) break;
     if (n <= need) {
-      for (int i = tid; i < n; i += kNT) emit(cand[i]);
+      for (int i = tid; i < n; i += NT) emit(cand[i]);
       break;
     }
     if (n <= 32) {
@@ -415,14 +417,14 @@ __device__ void block_select(unsigned long long* cand, unsigned long long* tmp, 
     const unsigned long long span = hi - lo;
     int shift = 0;
     if (span != 0ull) shift = max(0, 64 - __clzll((long long)span) - 8);
-    for (int i = tid; i < n; i += kNT) atomicAdd(&S.hist[bin_of(cand[i], lo, shift)], 1u);
+    for (int i = tid; i < n; i += NT) atomicAdd(&S.hist[bin_of(cand[i], lo, shift)], 1u);
     __syncthreads();
     boundary_bin(S, need);
     const uint32_t bs = (uint32_t)min(max(S.bstar, 0), 255);
     const int ab = S.above;
     const int nb = S.nb;
     int* tc = &S.tcnt[iter & 1];
-    for (int i = tid; i < n; i += kNT) {
+    for (int i = tid; i < n; i += NT) {
       const unsigned long long c = cand[i];
       const uint32_t b = bin_of(c, lo, shift);
       if (b > bs) {
@@ -433,7 +435,7 @@ __device__ void block_select(unsigned long long* cand, unsigned long long* tmp, 
       }
     }
     // ready for the next round: histogram cleared, the other counter reset
-    if (tid < 256) S.hist[tid] = 0u;
+    for (int q = tid; q < 256; q += NT) S.hist[q] = 0u;
     if (tid == 0) S.tcnt[(iter + 1) & 1] = 0;
     __syncthreads();
     need -= ab;

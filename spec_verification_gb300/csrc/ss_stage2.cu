@@ -2,7 +2,8 @@
 // verification (SonicSampler 3.1 "Speculative verification"; dl-note
 // "Rejection Sampler").
 //
-// One work item per target position (persistent CTAs of 256 threads):
+// One work item per target position (persistent CTAs of 128 threads, one
+// per candidate):
 //  1. merge: each of the position's segments (1..Z_v runs of tiles, one per
 //     stage-1 CTA) left its top-128 packed candidates in the staging buffer.
 //     One segment is the answer already; otherwise tau2 = the largest
@@ -31,6 +32,8 @@
 namespace ss {
 
 namespace {
+
+constexpr int kNT2 = 128;  // threads of a stage-2 CTA (one per candidate)
 
 struct S2Smem {
   SelectSmem sel;
@@ -105,7 +108,7 @@ __device__ __forceinline__ PosResult load_pos_result(const PosResult* p) {
 
 }  // namespace
 
-__global__ void __launch_bounds__(kNT) stage2_kernel(const Params P, int verify) {
+__global__ void __launch_bounds__(kNT2) stage2_kernel(const Params P, int verify) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   const int cap = P.Z * kK;
   unsigned long long* cand = reinterpret_cast<unsigned long long*>(smem_raw);
@@ -157,9 +160,9 @@ __global__ void __launch_bounds__(kNT) stage2_kernel(const Params P, int verify)
       }
     }
     uint32_t tst = 0u;
-    for (int t = tid; t < nseg; t += kNT) tst |= P.ws.tile_status[tbase + t];
+    for (int t = tid; t < nseg; t += kNT2) tst |= P.ws.tile_status[tbase + t];
     const unsigned long long* stg = P.ws.staging + tbase * kK;
-    for (int i = tid; i < nseg * kK; i += kNT) tmp[i] = stg[i];
+    for (int i = tid; i < nseg * kK; i += kNT2) tmp[i] = stg[i];
     __syncthreads();
     if (tst) atomicOr(&sm.status, tst);
     const int r = sm.r, j = sm.j, gamma = sm.gamma, c0 = sm.c0;
@@ -186,7 +189,7 @@ __global__ void __launch_bounds__(kNT) stage2_kernel(const Params P, int verify)
         if (tid < kK) sm.top[tid] = tid < need ? tmp[tid] : 0ull;
       } else {
         unsigned long long tm = 0ull;
-        for (int t = warp; t < nseg; t += kNT / 32) {
+        for (int t = warp; t < nseg; t += kNT2 / 32) {
           unsigned long long mn = ~0ull;
 #pragma unroll
           for (int q = 0; q < kK / 32; ++q) {
@@ -196,9 +199,9 @@ __global__ void __launch_bounds__(kNT) stage2_kernel(const Params P, int verify)
           mn = warp_min_u64(mn);
           tm = mn > tm ? mn : tm;
         }
-        const unsigned long long tau2 = block_max_u64(tm, sm.slots);
+        const unsigned long long tau2 = block_max_u64<kNT2>(tm, sm.slots);
         unsigned long long lmin = ~0ull, lmax = 0ull;
-        for (int i = tid; i < nseg * kK; i += kNT) {
+        for (int i = tid; i < nseg * kK; i += kNT2) {
           const unsigned long long c = tmp[i];
           if (c != 0ull && c >= tau2) {
             cand[atomicAdd(&sm.cnt, 1)] = c;
@@ -206,10 +209,10 @@ __global__ void __launch_bounds__(kNT) stage2_kernel(const Params P, int verify)
             lmax = c > lmax ? c : lmax;
           }
         }
-        const unsigned long long lo = block_min_u64(lmin, sm.slots);
-        const unsigned long long hi = block_max_u64(lmax, sm.slots);
+        const unsigned long long lo = block_min_u64<kNT2>(lmin, sm.slots);
+        const unsigned long long hi = block_max_u64<kNT2>(lmax, sm.slots);
         const int n = sm.cnt;
-        block_select(cand, tmp, n, need, lo, hi, sm.sel, [&](unsigned long long c) {
+        block_select<kNT2>(cand, tmp, n, need, lo, hi, sm.sel, [&](unsigned long long c) {
           const int s = atomicAdd(&sm.out_cnt, 1);
           if (s < kK) sm.top[s] = c;
         });
@@ -534,5 +537,7 @@ __global__ void __launch_bounds__(kNT) stage2_kernel(const Params P, int verify)
 }
 
 size_t stage2_smem_bytes(int Z) { return (size_t)Z * kK * 8 * 2 + sizeof(S2Smem); }
+
+int stage2_threads() { return kNT2; }
 
 }  // namespace ss
