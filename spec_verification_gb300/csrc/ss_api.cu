@@ -90,8 +90,7 @@ ss_status ss_plan_create(ss_plan** out, int32_t V, int32_t max_rows, int32_t max
     return fail(SS_ERR_ARG, "need 1 <= max_rows <= max_positions <= 2^24");
   if ((logits_dtype != SS_F32 && logits_dtype != SS_BF16) || (q_dtype != SS_F32 && q_dtype != SS_BF16))
     return fail(SS_ERR_ARG, "dtype must be SS_F32 or SS_BF16");
-  if (tile != 0 && tile != 4096 && tile != 8192 && tile != 16384)
-    return fail(SS_ERR_UNSUPPORTED, "tile must be 0, 4096, 8192 or 16384");
+  if (tile != 0 && tile != 8192 && tile != 16384) return fail(SS_ERR_UNSUPPORTED, "tile must be 0, 8192 or 16384");
   int ndev = 0;
   cudaError_t e = cudaGetDeviceCount(&ndev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDeviceCount");

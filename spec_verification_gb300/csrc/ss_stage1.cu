@@ -23,7 +23,7 @@
 //    (b) at least min(128, elements seen) buffer entries are >= cut.
 //    The segment's first stage takes the cut from the per-thread maxima (the
 //    16th largest of each warp's 32 maxima, minimum over the 8 warps, so 128
-//    maxima lie at or above it); afterwards a thread whose 16 elements all
+//    maxima lie at or above it); afterwards a thread whose 32 elements all
 //    fall below the cut does only the prelude and a NaN-propagating running
 //    maximum, and the rare elements at or above it are appended.  When the
 //    buffer passes kCompactAt entries it is cut back to its exact top-128,
@@ -60,8 +60,8 @@ constexpr int kHash = 1 << kHashBits;  // hash slots for a segment's history / b
 constexpr int kHashMax = 512;        // tokens a segment may list in the hash table
 constexpr int kBiasPre = 64;         // bias entries prefetched per segment
 constexpr int kPre = kNT;            // history / draft ids prefetched per segment
-constexpr int kPT = 16;              // elements per thread per chunk
-constexpr int kChunk = kPT * kNT;    // elements per chunk (a stage is 1..4 chunks)
+constexpr int kPT = 32;              // elements per thread per chunk
+constexpr int kChunk = kPT * kNT;    // elements per chunk (a stage is 1 or 2 chunks)
 constexpr float kLog2e = 1.4426950408889634f;
 
 static_assert(kCompactAt <= kCap - kK, "a stage fallback appends 128 entries after the rollback");
