@@ -26,8 +26,10 @@
 //    maxima lie at or above it); afterwards a thread whose 32 elements all
 //    fall below the cut does only the prelude and a NaN-propagating running
 //    maximum, and the rare elements at or above it are appended.  When the
-//    buffer passes kCompactAt entries it is cut back to its exact top-128,
-//    which raises the cut;
+//    buffer passes kRaiseAt entries one histogram pass raises the cut to the
+//    lower edge of the bin holding its 128th entry (dropping what lies
+//    below), or, if that frees too little, it is cut back to its exact
+//    top-128;
 //  - history / draft / bias tokens need their count and bias entries, so they
 //    are kept out of that path: per segment they are listed in a hash table
 //    (which the rare appends consult) and their exact values, read straight
@@ -54,7 +56,8 @@ namespace {
 constexpr int kSpinLimit = 1 << 22;  // bounded mbarrier wait (about a second)
 constexpr int kMaxSlots = 4;         // ring slots at most
 constexpr int kCap = 1024;           // candidate buffer entries
-constexpr int kCompactAt = 512;      // buffer fill that triggers a compaction (<= kCap - kK)
+constexpr int kRaiseAt = 384;        // buffer fill that triggers a cut raise
+constexpr int kCompactAt = 512;      // fill after a raise that triggers an exact compaction (<= kCap - kK)
 constexpr int kHashBits = 10;
 constexpr int kHash = 1 << kHashBits;  // hash slots for a segment's history / bias tokens
 constexpr int kHashMax = 512;        // tokens a segment may list in the hash table
@@ -330,6 +333,42 @@ __device__ __noinline__ unsigned long long compact(unsigned long long* cand, uns
   const unsigned long long c = t < kK ? outb[t] : ~0ull;
   if (t < kK) cand[t] = c;
   return block_min_u64(c, sm.slots);
+}
+
+// Raise the cut with one 256-bin histogram of the buffer over [cut, max]: the
+// new cut is the lower edge of the bin holding the 128th largest entry, so at
+// least 128 entries stay at or above it, and the entries below it leave the
+// buffer.  Returns the new cut (never below `cut`) and the new count in
+// sm.out_cnt.  Entries below `cut` (left by a stage fallback) count in bin 0.
+__device__ __noinline__ unsigned long long raise_cut(unsigned long long* cand, unsigned long long* tmp, int n,
+                                                     unsigned long long cut, S1Smem& sm) {
+  const int tid = threadIdx.x;
+  if (tid < 256) sm.sel.hist[tid] = 0u;
+  if (tid == 0) sm.out_cnt = 0;
+  unsigned long long mx = 0ull;
+  for (int i = tid; i < n; i += kNT) mx = cand[i] > mx ? cand[i] : mx;
+  mx = block_max_u64(mx, sm.slots);
+  const int shift = mx > cut ? max(0, 64 - __clzll((long long)(mx - cut)) - 8) : 0;
+  if (mx > cut)
+    for (int i = tid; i < n; i += kNT) atomicAdd(&sm.sel.hist[bin_of(cand[i], cut, shift)], 1u);
+  __syncthreads();
+  boundary_bin(sm.sel, kK);
+  const int bstar = mx > cut ? sm.sel.bstar : 0;
+  if (bstar <= 0) {  // no progress: keep everything
+    if (tid == 0) sm.out_cnt = n;
+    __syncthreads();
+    return cut;
+  }
+  const unsigned long long nc = cut + ((unsigned long long)bstar << shift);
+  for (int i = tid; i < n; i += kNT) {
+    const unsigned long long c = cand[i];
+    if (c >= nc) tmp[atomicAdd(&sm.out_cnt, 1)] = c;
+  }
+  __syncthreads();
+  const int m = sm.out_cnt;
+  for (int i = tid; i < m; i += kNT) cand[i] = tmp[i];
+  __syncthreads();
+  return nc;
 }
 
 // Load chunk ch of the stage and apply mask and temperature; returns the
@@ -817,10 +856,15 @@ __global__ void __launch_bounds__(kNT, 2) stage1_kernel(const Params P) {
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         issue(g + NS, slot);
       }
-      // ---- keep room in the buffer: exact top-128, which raises the cut
-      if (rc.valid && n_end > kCompactAt) {
-        cutp = compact(cand, tmp, outb, n_end, sm);
-        n_end = kK;
+      // ---- keep room in the buffer: one histogram pass raises the cut; the
+      // exact top-128 only if that left too many (a crowd of equal values)
+      if (rc.valid && n_end > kRaiseAt) {
+        cutp = raise_cut(cand, tmp, n_end, cutp, sm);
+        n_end = sm.out_cnt;
+        if (n_end > kCompactAt) {
+          cutp = compact(cand, tmp, outb, n_end, sm);
+          n_end = kK;
+        }
       }
       n = n_end;
       if (++slot == NS) {
