@@ -222,6 +222,23 @@ __device__ __forceinline__ int find_row(const int32_t* cu, int B, int pos) {
   return lo;
 }
 
+// The same by one warp: 32-way search rounds over the row offsets (every
+// lane calls and gets r).
+__device__ __forceinline__ int warp_find_row(const int32_t* cu, int B, int pos, int lane) {
+  int lo = 0, hi = B - 1;  // r in [lo, hi]; offset(lo) <= pos throughout
+  while (hi > lo) {
+    const int span = hi - lo + 1;
+    const int step = (span + 31) / 32;
+    const int idx = lo + lane * step;
+    const bool ok = idx <= hi && __ldg(cu + idx) + idx <= pos;
+    const uint32_t b = __ballot_sync(0xffffffffu, ok);
+    const int k = 31 - __clz((int)b);  // the last probe at or below pos (probe 0 always is)
+    lo = lo + k * step;
+    hi = min(hi, lo + step - 1);
+  }
+  return lo;
+}
+
 __device__ __forceinline__ int num_positions(const Params& P) {
   const int n = P.cu_draft ? (__ldg(P.cu_draft + P.B) + P.B) : P.B;
   return min(n, P.max_positions);

@@ -528,7 +528,7 @@ __global__ void __launch_bounds__(kNT, 2) stage1_kernel(const Params P) {
     const int pos = (int)(g0 / Z);
     int r = pos, c0 = 0, c1 = 0;
     if (P.cu_draft) {
-      r = find_row(P.cu_draft, P.B, pos);
+      r = warp_find_row(P.cu_draft, P.B, pos, lane);
       c0 = __ldg(P.cu_draft + r);
       c1 = __ldg(P.cu_draft + r + 1);
     }
@@ -574,6 +574,13 @@ __global__ void __launch_bounds__(kNT, 2) stage1_kernel(const Params P) {
     const ss_bias_entry* bl = (bias_on && rc.n_bias <= kBiasPre) ? cb.bias : brow;
 
     // ---- segment set-up: counters and the hash table of flagged tokens
+    float fl_raw[kHashMax / kNT];     // listed tokens' logits and mask words (hash mode)
+    uint32_t fl_mw[kHashMax / kNT];
+#pragma unroll
+    for (int k = 0; k < kHashMax / kNT; ++k) {
+      fl_raw[k] = 0.0f;
+      fl_mw[k] = 0xFFFFFFFFu;
+    }
     if (tid == 0) {
       sm.cnt[0] = sm.cnt[1] = sm.cnt[2] = 0;
       sm.nan_flag = 0;
@@ -624,39 +631,19 @@ __global__ void __launch_bounds__(kNT, 2) stage1_kernel(const Params P) {
           finfo[i] = hval[q];
         }
       __syncthreads();
-      // their exact processed values, read straight from HBM (all loads first),
-      // are the segment's first candidates
+      // their exact processed values, read straight from HBM, are the
+      // segment's first candidates: the loads go out now and are used once
+      // the first stage has been scanned
       const int nfl = sm.nf;
-      float raw[kHashMax / kNT];
-      uint32_t mw[kHashMax / kNT];
-#pragma unroll
-      for (int k = 0; k < kHashMax / kNT; ++k) {
-        const int i = tid + k * kNT;
-        raw[k] = 0.0f;
-        mw[k] = 0xFFFFFFFFu;
-        if (i < nfl) {
-          const int tok = ftok[i];
-          raw[k] = load_scalar(P.logits, P.logits_bf16, (int64_t)pos * P.ld + tok);
-          if (mask_on) mw[k] = __ldg(P.bitmask + (size_t)pos * P.mask_words + (tok >> 5));
-        }
-      }
-      bool nan_l = false;
 #pragma unroll
       for (int k = 0; k < kHashMax / kNT; ++k) {
         const int i = tid + k * kNT;
         if (i < nfl) {
           const int tok = ftok[i];
-          const uint32_t info = finfo[i];
-          float v = raw[k];
-          if (((mw[k] >> (tok & 31)) & 1u) == 0u) v = -INFINITY;
-          v = apply_penalty_bias(v, info & 0x7FFFFFFFu, (info >> 31) != 0u, tok, rc, bl);
-          v = __fmul_rn(v, rc.rT);
-          nan_l |= v != v;
-          cand[i] = pack(v != v ? kKeyNegInf : f2key(v), (uint32_t)tok);
+          fl_raw[k] = load_scalar(P.logits, P.logits_bf16, (int64_t)pos * P.ld + tok);
+          if (mask_on) fl_mw[k] = __ldg(P.bitmask + (size_t)pos * P.mask_words + (tok >> 5));
         }
       }
-      if (nan_l) sm.nan_flag = 1;
-      __syncthreads();
     }
     const int nf = hashed ? sm.nf : 0;
 
@@ -708,9 +695,33 @@ __global__ void __launch_bounds__(kNT, 2) stage1_kernel(const Params P) {
         // pass 0 (a segment's first stage only): the cut from the per-thread
         // maxima; pass 1: the stream (prelude, running maximum, rare appends)
         bool nan_seen = false;
-        for (int pass = first ? 0 : 1; pass < 2; ++pass) {
-          const uint32_t ck = pk_key(cutp);
-          const float cut_f = ck <= kKeyNegInf ? -INFINITY : key2f(ck);
+        // the first stage's cut: the 16th largest of each warp's 32 thread
+        // maxima (bitonic sort across lanes), minimum over the warps, so at
+        // least 8 * 16 elements are >= it
+        auto certify = [&](float mt) -> unsigned long long {
+          float v = mt;
+#pragma unroll
+          for (int kk = 2; kk <= 32; kk <<= 1) {
+#pragma unroll
+            for (int d = kk >> 1; d > 0; d >>= 1) {
+              const float o = __shfl_xor_sync(0xffffffffu, v, d);
+              const bool keep_max = (((lane & d) == 0) == ((lane & kk) == 0));
+              v = keep_max ? fmaxf(v, o) : fminf(v, o);
+            }
+          }
+          if (lane == 15) sm.tw[warp] = v;
+          __syncthreads();
+          float tau = sm.tw[0];
+#pragma unroll
+          for (int w = 1; w < kNT / 32; ++w) tau = fminf(tau, sm.tw[w]);
+          return pack(f2key(tau), 0xFFFFFFFFu);  // every element >= tau
+        };
+        // a one-chunk first stage takes the cut from the chunk it holds;
+        // otherwise pass 0 scans the stage for the maxima first
+        const bool merged = first && nch == 1;
+        for (int pass = (first && !merged) ? 0 : 1; pass < 2; ++pass) {
+          uint32_t ck = pk_key(cutp);
+          float cut_f = ck <= kKeyNegInf ? -INFINITY : key2f(ck);
           float mt = -INFINITY;
           for (int ch = 0; ch < nch; ++ch) {
             float x[kPT];
@@ -719,6 +730,17 @@ __global__ void __launch_bounds__(kNT, 2) stage1_kernel(const Params P) {
 #pragma unroll
               for (int e = 0; e < kPT; ++e) mt = fmaxf(mt, x[e]);
               continue;
+            }
+            if (merged) {
+              float mc = m;
+              if (mc != mc) {  // NaN among them: the maximum of the rest
+                mc = -INFINITY;
+#pragma unroll
+                for (int e = 0; e < kPT; ++e) mc = fmaxf(mc, x[e]);
+              }
+              cutp = certify(mc);
+              ck = pk_key(cutp);
+              cut_f = ck <= kKeyNegInf ? -INFINITY : key2f(ck);
             }
             if (!(m < cut_f)) {
               // elements at or above the cut (or NaN): re-derived from the slot
@@ -760,25 +782,24 @@ __global__ void __launch_bounds__(kNT, 2) stage1_kernel(const Params P) {
               }
             }
           }
-          if (pass == 0) {
-            // 16th largest of the warp's 32 maxima (bitonic sort across lanes);
-            // tau = the minimum over warps, so >= 8 * 16 elements are >= tau
-            float v = mt;
+          if (pass == 0) cutp = certify(mt);
+        }
+        // the listed tokens' exact values (hash mode), from the loads issued at set-up
+        if (first && hashed) {
+          const int nfl = nf;
 #pragma unroll
-            for (int kk = 2; kk <= 32; kk <<= 1) {
-#pragma unroll
-              for (int d = kk >> 1; d > 0; d >>= 1) {
-                const float o = __shfl_xor_sync(0xffffffffu, v, d);
-                const bool keep_max = (((lane & d) == 0) == ((lane & kk) == 0));
-                v = keep_max ? fmaxf(v, o) : fminf(v, o);
-              }
+          for (int k = 0; k < kHashMax / kNT; ++k) {
+            const int i = tid + k * kNT;
+            if (i < nfl) {
+              const int tok = ftok[i];
+              const uint32_t info = finfo[i];
+              float v = fl_raw[k];
+              if (((fl_mw[k] >> (tok & 31)) & 1u) == 0u) v = -INFINITY;
+              v = apply_penalty_bias(v, info & 0x7FFFFFFFu, (info >> 31) != 0u, tok, rc, bl);
+              v = __fmul_rn(v, rc.rT);
+              nan_seen |= v != v;
+              cand[i] = pack(v != v ? kKeyNegInf : f2key(v), (uint32_t)tok);
             }
-            if (lane == 15) sm.tw[warp] = v;
-            __syncthreads();
-            float tau = sm.tw[0];
-#pragma unroll
-            for (int w = 1; w < kNT / 32; ++w) tau = fminf(tau, sm.tw[w]);
-            cutp = pack(f2key(tau), 0xFFFFFFFFu);  // every element >= tau
           }
         }
 

@@ -47,23 +47,6 @@ struct S2Smem {
   uint32_t status;
 };
 
-// Row of target position pos (the largest r with cu[r] + r <= pos) by one
-// warp: 32-way search rounds over the row offsets.  Every lane gets r.
-__device__ __forceinline__ int warp_find_row(const int32_t* cu, int B, int pos, int lane) {
-  int lo = 0, hi = B - 1;  // r in [lo, hi]; offset(lo) <= pos throughout
-  while (hi > lo) {
-    const int span = hi - lo + 1;
-    const int step = (span + 31) / 32;
-    const int idx = lo + lane * step;
-    const bool ok = idx <= hi && __ldg(cu + idx) + idx <= pos;
-    const uint32_t b = __ballot_sync(0xffffffffu, ok);
-    const int k = 31 - __clz((int)b);  // the last probe at or below pos (probe 0 always is)
-    lo = lo + k * step;
-    hi = min(hi, lo + step - 1);
-  }
-  return lo;
-}
-
 // Processed logit of one token at one position (the same fp32 steps as the
 // stage-1 prelude), for a draft token outside the candidate list.  One warp.
 __device__ float prelude_single_warp(const Params& P, const RowCtx& rc, int pos, int r, int c0, int jn, int tok,
