@@ -256,28 +256,9 @@ ss_status launch(const ss_plan* pl, const ss::Params& P, cudaStream_t st, bool v
   rec(0);
   ss::stage1_launch(pl->ldt == SS_BF16, pl->grid1, pl->smem1, st, P);
   rec(1);
-  // stage 2 and the residual pass are launched as programmatic dependents:
-  // they may be scheduled while the previous kernel drains and wait for its
-  // results (griddepcontrol.wait) before reading them
-  cudaLaunchAttribute pdl[1];
-  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  pdl[0].val.programmaticStreamSerializationAllowed = 1;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)pl->grid2);
-  cfg.blockDim = dim3((unsigned)ss::stage2_threads());
-  cfg.dynamicSmemBytes = pl->smem2;
-  cfg.stream = st;
-  cfg.attrs = pdl;
-  cfg.numAttrs = 1;
-  cudaError_t le = cudaLaunchKernelEx(&cfg, ss::stage2_kernel, P, verify ? 1 : 0);
+  ss::stage2_kernel<<<pl->grid2, ss::stage2_threads(), pl->smem2, st>>>(P, verify ? 1 : 0);
   rec(2);
-  if (verify && le == cudaSuccess) {
-    cfg.gridDim = dim3((unsigned)pl->grid3);
-    cfg.blockDim = dim3((unsigned)ss::kNT);
-    cfg.dynamicSmemBytes = pl->smem3;
-    le = cudaLaunchKernelEx(&cfg, ss::residual_kernel, P);
-  }
-  if (le != cudaSuccess) return cuda_fail(le, "kernel launch");
+  if (verify) ss::residual_kernel<<<pl->grid3, ss::kNT, pl->smem3, st>>>(P);
   rec(3);
   if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
   e = cudaGetLastError();

@@ -82,7 +82,6 @@ __device__ void build_aux(const Params& P, const RowCtx& rc, int r, int j, int t
 
 __global__ void __launch_bounds__(kNT) residual_kernel(const Params P) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  cudaGridDependencySynchronize();  // stage 2's queue and position results
   uint16_t* aux = reinterpret_cast<uint16_t*>(smem_raw);
   S3Smem& sm = *reinterpret_cast<S3Smem*>(smem_raw + (size_t)P.BN * 2);
   const int tid = threadIdx.x;

@@ -462,9 +462,6 @@ __global__ void __launch_bounds__(kNT, 2) stage1_kernel(const Params P) {
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int V = P.V, Z = P.Z;
-  // stage 2 may be scheduled once every stage-1 CTA is running (it waits for
-  // this grid's completion before it reads anything)
-  cudaTriggerProgrammaticLaunchCompletion();
   if (blockIdx.x == 0 && tid == 0) *P.ws.resid_count = 0u;  // residual queue of this call
   const int npos = num_positions(P);
   const long long T = (long long)npos * Z;

@@ -93,10 +93,6 @@ __device__ __forceinline__ PosResult load_pos_result(const PosResult* p) {
 
 __global__ void __launch_bounds__(kNT2) stage2_kernel(const Params P, int verify) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  // launched as a programmatic dependent of stage 1: let the residual pass be
-  // scheduled early, then wait for stage 1's lists
-  cudaTriggerProgrammaticLaunchCompletion();
-  cudaGridDependencySynchronize();
   const int cap = P.Z * kK;
   unsigned long long* cand = reinterpret_cast<unsigned long long*>(smem_raw);
   unsigned long long* tmp = cand + cap;
