@@ -420,6 +420,63 @@ __device__ __forceinline__ float load_chunk_sel(bool mask, bool full, const unsi
               : load_chunk<BF16, false, false>(ring, msl, rT, ch, nt, x);
 }
 
+// Vector v of chunk ch of a full stage with mask and temperature applied
+// (the same fp32 steps as load_chunk, so the same bits).
+template <bool BF16, bool MASK>
+__device__ __forceinline__ void load_vec(const unsigned char* ring, const uint32_t* msl, float rT, int ch, int v,
+                                         float* y) {
+  constexpr int VEC = BF16 ? 8 : 4;
+  const int e0 = elem_index<VEC>(ch, v, 0);
+  const uint4 raw = *reinterpret_cast<const uint4*>(ring + (size_t)e0 * (BF16 ? 2 : 4));
+  uint32_t bits = 0xFFFFFFFFu;
+  if constexpr (MASK) bits = msl[e0 >> 5] >> (e0 & 31);
+#pragma unroll
+  for (int jj = 0; jj < VEC; ++jj) {
+    float val = vec_elem<BF16>(raw, jj);
+    if constexpr (MASK) {
+      if (((bits >> jj) & 1u) == 0u) val = -INFINITY;
+    }
+    y[jj] = __fmul_rn(val, rT);
+  }
+}
+
+__device__ __forceinline__ uint32_t bf16x2_max_nan(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// NaN-propagating maxima of the RAW values of chunk ch (no mask, no
+// temperature), per vector in vm and overall.  For rT > 0, rounding x * rT is
+// monotone in x, so a chunk whose raw maximum m has fl(m * rT) below the cut
+// holds no processed value at or above it (masked values are -inf); with
+// rT = +inf, m >= 0 gives +inf or NaN and the chunk is examined.
+template <bool BF16>
+__device__ __forceinline__ float raw_chunk_max(const unsigned char* ring, int ch, float (&vm)[kPT / (BF16 ? 8 : 4)]) {
+  constexpr int VEC = BF16 ? 8 : 4;
+  constexpr int NV = kPT / VEC;
+#pragma unroll
+  for (int v = 0; v < NV; ++v) {
+    const int e0 = elem_index<VEC>(ch, v, 0);
+    const uint4 raw = *reinterpret_cast<const uint4*>(ring + (size_t)e0 * (BF16 ? 2 : 4));
+    if constexpr (BF16) {
+      const uint32_t c = bf16x2_max_nan(bf16x2_max_nan(raw.x, raw.y), bf16x2_max_nan(raw.z, raw.w));
+      vm[v] = fmax_nan(bf16_lo(c), bf16_hi(c));
+    } else {
+      vm[v] = fmax_nan(fmax_nan(__uint_as_float(raw.x), __uint_as_float(raw.y)),
+                       fmax_nan(__uint_as_float(raw.z), __uint_as_float(raw.w)));
+    }
+  }
+  float t[NV];
+#pragma unroll
+  for (int v = 0; v < NV; ++v) t[v] = vm[v];
+#pragma unroll
+  for (int w = NV / 2; w >= 1; w >>= 1)
+#pragma unroll
+    for (int e = 0; e < w; ++e) t[e] = fmax_nan(t[e], t[e + w]);
+  return t[0];
+}
+
 // The value the stream computes for stage element li (mask and temperature:
 // the same fp32 steps as load_chunk, so the same bits).
 template <bool BF16>
@@ -719,11 +776,50 @@ __global__ void __launch_bounds__(kNT, 2) stage1_kernel(const Params P) {
         // a one-chunk first stage takes the cut from the chunk it holds;
         // otherwise pass 0 scans the stage for the maxima first
         const bool merged = first && nch == 1;
+        const bool lazy = !first && full && !lse_on;
         for (int pass = (first && !merged) ? 0 : 1; pass < 2; ++pass) {
           uint32_t ck = pk_key(cutp);
           float cut_f = ck <= kKeyNegInf ? -INFINITY : key2f(ck);
           float mt = -INFINITY;
           for (int ch = 0; ch < nch; ++ch) {
+            if (lazy) {
+              // a full stage after the segment's first: the raw maxima decide,
+              // and only the vectors that may hold a hit are processed
+              float vm[NV];
+              const float m = raw_chunk_max<BF16>(ring, ch, vm);
+              if (!(__fmul_rn(m, rc.rT) < cut_f)) {
+                uint32_t vb = 0u;
+#pragma unroll
+                for (int v = 0; v < NV; ++v) vb |= (__fmul_rn(vm[v], rc.rT) < cut_f ? 0u : 1u) << v;
+                while (vb) {
+                  const int v = __ffs((int)vb) - 1;
+                  vb &= vb - 1u;
+                  float y[VEC];
+                  if (mask_on) load_vec<BF16, true>(ring, msl, rc.rT, ch, v, y);
+                  else load_vec<BF16, false>(ring, msl, rc.rT, ch, v, y);
+                  uint32_t bits = 0u;
+#pragma unroll
+                  for (int jj = 0; jj < VEC; ++jj) bits |= (y[jj] < cut_f ? 0u : 1u) << jj;
+                  const int e0 = elem_index<VEC>(ch, v, 0);
+                  while (bits) {
+                    const int jj = __ffs((int)bits) - 1;
+                    bits &= bits - 1u;
+                    float xv = y[0];
+#pragma unroll
+                    for (int k = 1; k < VEC; ++k) xv = jj == k ? y[k] : xv;
+                    const int li = e0 + jj;
+                    const bool isn = xv != xv;
+                    nan_seen |= isn;
+                    const unsigned long long pk = pack(isn ? kKeyNegInf : f2key(xv), (uint32_t)(t0 + li));
+                    bool fl = false;
+                    if (hashed) fl = hash_find(hkey, t0 + li) >= 0;
+                    else if (staged) fl = aux[li] != 0u;
+                    if (pk >= cutp && !fl) append(pk);
+                  }
+                }
+              }
+              continue;
+            }
             float x[kPT];
             const float m = load_chunk_sel<BF16>(mask_on, full, ring, msl, rc.rT, ch, nt, x);
             if (pass == 0) {
