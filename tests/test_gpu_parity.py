@@ -112,6 +112,49 @@ def test_nan_inf_and_masked_rows():
         check(w)
 
 
+def _allowed(mask_row, tok):
+    return (int(mask_row[tok >> 5]) >> (tok & 31)) & 1
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_late_stage_nan_inf_and_masked_extremes(dtype):
+    # 96 rows x 13 stages is more stages than stage-1 CTAs, so segments run
+    # over several stages and the stages after a segment's first are filtered
+    # on raw (unmasked, untempered) maxima: values hidden by the mask, NaN and
+    # inf planted past the first stage, all-negative rows and an infinite 1/T
+    rng = np.random.default_rng(12)
+    B, V = 96, 100003
+    x = rng.normal(0.0, 1.5, (B, V)).astype(np.float32)
+    mask = W.bool_to_mask_bits(rng.random((B, V)) < 0.6)
+    late = np.arange(40000, V)
+
+    def pick(r, allowed, n):
+        c = [t for t in rng.permutation(late)[:4 * n + 64] if _allowed(mask[r], int(t)) == allowed]
+        return np.asarray(c[:n], np.int64)
+
+    for r in range(0, 4):                  # NaN where the mask hides it: no NaN status
+        x[r, pick(r, 0, 50)] = np.nan
+    for r in range(4, 6):                  # one visible NaN in a late stage
+        x[r, pick(r, 1, 1)] = np.nan
+    for r in range(6, 8):                  # visible +inf in a late stage: a point mass
+        x[r, pick(r, 1, 1)] = np.inf
+    for r in range(8, 10):                 # huge values and +inf hidden by the mask
+        x[r, pick(r, 0, 20)] = 1e30
+        x[r, pick(r, 0, 3)] = np.inf
+    x[10:12] -= 40.0                       # every value negative
+    x[12] = -np.abs(x[12]) - 0.5           # 1/T = +inf: one positive value left
+    tpos = int(pick(12, 1, 1)[0])
+    x[12, tpos] = 2.0
+    x[13, 90000:98000] += 8.0              # the row's top values all in one late stage
+    temp = np.ones(B, np.float32)
+    temp[12] = np.float32(1e-40)           # subnormal, RN(1/T) = +inf
+    fl = F.MASK | F.TOPK | F.TOPP | F.MINP
+    w = sample_case(x, flags=fl, dtype=dtype, bitmask=mask, top_k=64, top_p=0.9, min_p=0.02,
+                    temperature=temp)
+    gpu, ora, _ = check(w)
+    assert gpu["tokens"][12] == tpos
+
+
 def test_bad_params_and_ids():
     rng = np.random.default_rng(3)
     V = 9000
