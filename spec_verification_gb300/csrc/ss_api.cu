@@ -7,6 +7,7 @@
 #include <cstring>
 #include <new>
 #include <string>
+#include <vector>
 
 #include "ss.h"
 #include "ss_common.cuh"
@@ -27,6 +28,7 @@ struct ss_plan {
   int V, max_rows, max_positions, BN, Z, device, sms, nslot;
   ss_dtype ldt, qdt;
   int grid1, grid2, grid3;
+  std::vector<int> grid2_by_cap;  // stage-2 grid for a shared-memory capacity of c lists (index c)
   size_t smem1, smem2, smem3;
   const void* k1;
   size_t off_staging, off_tlse, off_tst, off_pos, off_rowc, off_rescnt, off_res, off_diag, ws_bytes;
@@ -158,6 +160,18 @@ ss_status ss_plan_create(ss_plan** out, int32_t V, int32_t max_rows, int32_t max
   const long long items1 = (long long)max_positions * p->Z;
   p->grid1 = (int)std::min<long long>(items1, (long long)std::max(occ1, 1) * sms);
   p->grid2 = std::min(max_positions, std::max(occ2, 1) * sms);
+  // stage 2 sized per call by the lists a position can have (ss::seg_cap_for)
+  p->grid2_by_cap.assign(p->Z + 1, p->grid2);
+  for (int c = 1; c < p->Z && e == cudaSuccess; ++c) {
+    int o = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, ss::stage2_kernel, ss::stage2_threads(),
+                                                      ss::stage2_smem_bytes(c));
+    p->grid2_by_cap[c] = std::min(max_positions, std::max(o, 1) * sms);
+  }
+  if (e != cudaSuccess) {
+    delete p;
+    return cuda_fail(e, "kernel attributes");
+  }
   p->grid3 = (int)std::min<long long>((long long)max_rows * p->Z, (long long)std::max(occ3, 1) * sms);
 
   // workspace layout (256-byte aligned regions)
@@ -239,7 +253,23 @@ int mask_rows_copyable(const ss::Params& P) {
   return P.bitmask != nullptr && aligned16(P.bitmask) && P.mask_words % 4 == 0 ? 1 : 0;
 }
 
-ss_status launch(const ss_plan* pl, const ss::Params& P, cudaStream_t st, bool verify, void* const* ev) {
+// Segment lists stage 2 must hold for one position.  A position's Z_v stages
+// meet at most 1 + ceil((Z_v - 1) / L) stage-1 ranges when every range has at
+// least L stages.  A call has at least B positions (exactly B when sampling),
+// and once B * Z_v >= grid1 the ranges are at least floor(B * Z_v / grid1)
+// stages long; below that a range may be a single stage.
+int seg_cap_for(const ss_plan* pl, int B) {
+  const long long tmin = (long long)std::min(B, pl->max_positions) * pl->Z;
+  if (tmin < pl->grid1) return pl->Z;
+  const long long L = tmin / pl->grid1;
+  return (int)std::min<long long>(pl->Z, 1 + (pl->Z - 1 + L - 1) / L);
+}
+
+ss_status launch(const ss_plan* pl, const ss::Params& P0, cudaStream_t st, bool verify, void* const* ev) {
+  ss::Params P = P0;
+  P.seg_cap = seg_cap_for(pl, P.B);
+  const size_t smem2 = ss::stage2_smem_bytes(P.seg_cap);
+  const int grid2 = pl->grid2_by_cap[P.seg_cap];
   cudaError_t e = cudaSuccess;
   // Under stream capture a plain event record is only a fork/join marker;
   // the external flag makes it an event-record node that fires at replay.
@@ -256,7 +286,7 @@ ss_status launch(const ss_plan* pl, const ss::Params& P, cudaStream_t st, bool v
   rec(0);
   ss::stage1_launch(pl->ldt == SS_BF16, pl->grid1, pl->smem1, st, P);
   rec(1);
-  ss::stage2_kernel<<<pl->grid2, ss::stage2_threads(), pl->smem2, st>>>(P, verify ? 1 : 0);
+  ss::stage2_kernel<<<grid2, ss::stage2_threads(), smem2, st>>>(P, verify ? 1 : 0);
   rec(2);
   if (verify) ss::residual_kernel<<<pl->grid3, ss::kNT, pl->smem3, st>>>(P);
   rec(3);

@@ -68,6 +68,7 @@ struct Params {
   int max_positions;
   int grid1;                // CTAs of the stage-1 launch (fixes the segment split)
   int nslot;                // stage-1 ring slots
+  int seg_cap;              // segment lists per position that stage 2's shared memory holds
   int mask_tma;             // bitmask rows can be bulk-copied (16-byte aligned rows)
   Workspace ws;
   ss_out out;

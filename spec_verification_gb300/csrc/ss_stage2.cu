@@ -91,9 +91,9 @@ __device__ __forceinline__ PosResult load_pos_result(const PosResult* p) {
 
 }  // namespace
 
-__global__ void __launch_bounds__(kNT2) stage2_kernel(const Params P, int verify) {
+__global__ void __launch_bounds__(kNT2, 9) stage2_kernel(const Params P, int verify) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  const int cap = P.Z * kK;
+  const int cap = P.seg_cap * kK;  // the lists of one position (at most seg_cap of them)
   unsigned long long* cand = reinterpret_cast<unsigned long long*>(smem_raw);
   unsigned long long* tmp = cand + cap;
   S2Smem& sm = *reinterpret_cast<S2Smem*>(tmp + cap);
@@ -144,12 +144,20 @@ __global__ void __launch_bounds__(kNT2) stage2_kernel(const Params P, int verify
     }
     uint32_t tst = 0u;
     for (int t = tid; t < nseg; t += kNT2) tst |= P.ws.tile_status[tbase + t];
+    // the host sizes seg_cap so that no position has more lists; should that
+    // bound ever fail, the position is reported as invalid rather than merged
+    const bool fits = nseg <= P.seg_cap;
     const unsigned long long* stg = P.ws.staging + tbase * kK;
-    for (int i = tid; i < nseg * kK; i += kNT2) tmp[i] = stg[i];
+    if (fits)
+      for (int i = tid; i < nseg * kK; i += kNT2) tmp[i] = stg[i];
     __syncthreads();
     if (tst) atomicOr(&sm.status, tst);
     const int r = sm.r, j = sm.j, gamma = sm.gamma, c0 = sm.c0;
-    const RowCtx rc = make_row(P.rows[r], P.hist_stride, P.bias_stride);
+    RowCtx rc = make_row(P.rows[r], P.hist_stride, P.bias_stride);
+    if (!fits) {
+      rc.valid = false;
+      if (tid == 0) atomicAdd(P.ws.diag + 1, 1u);
+    }
     const uint32_t position = rc.position + (uint32_t)j;
     const uint64_t seed = P.seeds[r];
     const bool is_draft = verify && j >= 0 && j < gamma;
