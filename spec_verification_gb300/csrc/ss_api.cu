@@ -172,7 +172,10 @@ ss_status ss_plan_create(ss_plan** out, int32_t V, int32_t max_rows, int32_t max
     delete p;
     return cuda_fail(e, "kernel attributes");
   }
-  p->grid3 = (int)std::min<long long>((long long)max_rows * p->Z, (long long)std::max(occ3, 1) * sms);
+  // residual items are (entry, 1024-token piece); at most four CTAs per SM so
+  // that a call with no rejection spends little on empty CTAs
+  const long long items3 = (long long)max_rows * ((V + 4 * ss::kNT - 1) / (4 * ss::kNT));
+  p->grid3 = (int)std::min<long long>(items3, (long long)std::min(std::max(occ3, 1), 4) * sms);
 
   // workspace layout (256-byte aligned regions)
   size_t off = 0;

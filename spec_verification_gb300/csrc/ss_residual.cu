@@ -4,18 +4,20 @@
 //
 // The row walk of stage 2 queues (row, rejected draft index, target position)
 // entries.  This kernel has a fixed launch shape (persistent CTAs) and loops
-// over (entry, vocabulary tile) items: each tile recomputes the processed
+// over (entry, 1024-token piece) items: each piece recomputes the processed
 // logits with the stage-1 prelude, p_i = exp(l_i - LSE) with the LSE stage 2
 // assembled from the tiles' (max, sum exp) partials, r_i = p_i - q_i, and the
-// Gumbel-max score ln r_i + g_i (Philox purpose 2) over r_i > 0.  Tiles combine
-// by a 64-bit atomicMax of (key(score) << 32 | ~token); the last tile of an
-// entry writes the token.  If no r_i is positive, the last tile draws from p
-// itself (Gumbel-max of l_i + g_i over the vocabulary).
+// Gumbel-max score ln r_i + g_i (Philox purpose 2) over r_i > 0.  Pieces
+// combine by a 64-bit atomicMax of (key(score) << 32 | ~token); the last piece
+// of an entry writes the token.  If no r_i is positive, the last piece draws
+// from p itself (Gumbel-max of l_i + g_i over the vocabulary, by B_N tiles).
 #include "ss_common.cuh"
 
 namespace ss {
 
 namespace {
+
+constexpr int kSub = 4 * kNT;  // tokens per work item: one group of 4 per thread
 
 struct S3Smem {
   unsigned long long slots[kNT / 32];
@@ -80,17 +82,20 @@ __device__ void build_aux(const Params& P, const RowCtx& rc, int r, int j, int t
 
 }  // namespace
 
-__global__ void __launch_bounds__(kNT) residual_kernel(const Params P) {
+__global__ void __launch_bounds__(kNT, 4) residual_kernel(const Params P) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   uint16_t* aux = reinterpret_cast<uint16_t*>(smem_raw);
   S3Smem& sm = *reinterpret_cast<S3Smem*>(smem_raw + (size_t)P.BN * 2);
   const int tid = threadIdx.x;
   const int Z = P.Z, V = P.V;
   const int count = (int)__ldcg(P.ws.resid_count);
-  const long long total = (long long)count * Z;
+  // items are (entry, kSub-token piece): an entry's pieces run on many CTAs,
+  // so a handful of rejections still spreads over the whole GPU
+  const int nsub = (V + kSub - 1) / kSub;
+  const long long total = (long long)count * nsub;
   for (long long item = blockIdx.x; item < total; item += gridDim.x) {
-    const int e = (int)(item / Z);
-    const int tile = (int)(item - (long long)e * Z);
+    const int e = (int)(item / nsub);
+    const int piece = (int)(item - (long long)e * nsub);
     ResidEntry* ent = P.ws.resid + e;
     const int r = __ldcg(&ent->row), j = __ldcg(&ent->j), pos = __ldcg(&ent->pos);
     const RowCtx rc = make_row(P.rows[r], P.hist_stride, P.bias_stride);
@@ -102,8 +107,8 @@ __global__ void __launch_bounds__(kNT) residual_kernel(const Params P) {
     const bool bias_on = (rc.flags & SS_BIAS) && P.bias != nullptr;
     const bool aux_on = pen_on || bias_on;
     const ss_bias_entry* brow = bias_on ? P.bias + (size_t)r * P.bias_stride : nullptr;
-    const int t0 = tile * P.BN;
-    const int nt = min(P.BN, V - t0);
+    const int t0 = piece * kSub;
+    const int nt = min(kSub, V - t0);
     if (tid == 0) sm.last = 0;
     if (aux_on) build_aux(P, rc, r, j, t0, nt, aux, pen_on, bias_on, brow);
     else __syncthreads();
@@ -142,7 +147,7 @@ __global__ void __launch_bounds__(kNT) residual_kernel(const Params P) {
       if (best) atomicMax(&ent->best, best);
       __threadfence();
       const uint32_t old = atomicAdd(&ent->arrivals, 1u);
-      sm.last = (old == (uint32_t)(Z - 1)) ? 1 : 0;
+      sm.last = (old == (uint32_t)(nsub - 1)) ? 1 : 0;
     }
     __syncthreads();
     if (sm.last) {
