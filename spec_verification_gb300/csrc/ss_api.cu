@@ -22,6 +22,7 @@ int stage1_max_slots();
 size_t stage2_smem_bytes(int Z);
 int stage2_threads();
 size_t residual_smem_bytes(int BN);
+int residual_piece_tokens();
 }  // namespace ss
 
 struct ss_plan {
@@ -172,9 +173,10 @@ ss_status ss_plan_create(ss_plan** out, int32_t V, int32_t max_rows, int32_t max
     delete p;
     return cuda_fail(e, "kernel attributes");
   }
-  // residual items are (entry, 1024-token piece); at most four CTAs per SM so
+  // residual items are (entry, vocabulary piece); at most four CTAs per SM so
   // that a call with no rejection spends little on empty CTAs
-  const long long items3 = (long long)max_rows * ((V + 4 * ss::kNT - 1) / (4 * ss::kNT));
+  const int piece = ss::residual_piece_tokens();
+  const long long items3 = (long long)max_rows * ((V + piece - 1) / piece);
   p->grid3 = (int)std::min<long long>(items3, (long long)std::min(std::max(occ3, 1), 4) * sms);
 
   // workspace layout (256-byte aligned regions)

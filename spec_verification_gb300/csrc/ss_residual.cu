@@ -4,7 +4,7 @@
 //
 // The row walk of stage 2 queues (row, rejected draft index, target position)
 // entries.  This kernel has a fixed launch shape (persistent CTAs) and loops
-// over (entry, 1024-token piece) items: each piece recomputes the processed
+// over (entry, 2048-token piece) items: each piece recomputes the processed
 // logits with the stage-1 prelude, p_i = exp(l_i - LSE) with the LSE stage 2
 // assembled from the tiles' (max, sum exp) partials, r_i = p_i - q_i, and the
 // Gumbel-max score ln r_i + g_i (Philox purpose 2) over r_i > 0.  Pieces
@@ -17,7 +17,7 @@ namespace ss {
 
 namespace {
 
-constexpr int kSub = 4 * kNT;  // tokens per work item: one group of 4 per thread
+constexpr int kSub = 8 * kNT;  // tokens per work item: two groups of 4 per thread
 
 struct S3Smem {
   unsigned long long slots[kNT / 32];
@@ -198,5 +198,7 @@ __global__ void __launch_bounds__(kNT, 4) residual_kernel(const Params P) {
 }
 
 size_t residual_smem_bytes(int BN) { return (size_t)BN * 2 + sizeof(S3Smem) + 16; }
+
+int residual_piece_tokens() { return kSub; }
 
 }  // namespace ss

@@ -40,6 +40,7 @@ struct S2Smem {
   unsigned long long top[kK];  // the selected candidates (unordered)
   unsigned long long srt[kK];  // the same, ordered
   double w[kK];                // exp(l_t - l_0) of the ordered candidates (stochastic rows)
+  float g[kK];                 // their Gumbel noise: sample (purpose 0) or residual (purpose 2)
   unsigned long long slots[kNT / 32];
   double lse;
   int r, j, gamma, c0, cnt, out_cnt, last, token, accept, d;
@@ -230,6 +231,10 @@ __global__ void __launch_bounds__(kNT2, 9) stage2_kernel(const Params P, int ver
         const float lt = (tid < need && c != 0ull) ? key2f(pk_key(c)) : -INFINITY;
         const float lz = key2f(pk_key(sm.srt[0]));
         sm.w[tid] = (rc.stoch && lt > -INFINITY && lz < INFINITY) ? exp((double)lt - (double)lz) : 0.0;
+        // the candidate's Gumbel noise, one Philox draw per thread: the sample
+        // of a sampled / bonus position, or the truncated residual's of a draft
+        if (rc.stoch && (!is_draft || rc.trunc) && tid < need && c != 0ull)
+          sm.g[tid] = gumbel_of(philox_uniform(seed, (uint32_t)pk_tok(c), position, (uint32_t)r, is_draft ? 2u : 0u));
       }
       __syncthreads();
 
@@ -338,7 +343,7 @@ __global__ void __launch_bounds__(kNT2, 9) stage2_kernel(const Params P, int ver
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
               if (4 * lane + k < nk) {
-                const float g = gumbel_of(philox_uniform(seed, (uint32_t)tok[k], position, (uint32_t)r, 0u));
+                const float g = sm.g[4 * lane + k];
                 const unsigned long long s = pack(f2key(__fadd_rn(l[k], g)), (uint32_t)tok[k]);
                 sc = s > sc ? s : sc;
               }
@@ -416,7 +421,7 @@ __global__ void __launch_bounds__(kNT2, 9) stage2_kernel(const Params P, int ver
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
                   if (4 * lane + k < nk) {
-                    const float g = gumbel_of(philox_uniform(seed, (uint32_t)tok[k], position, (uint32_t)r, 2u));
+                    const float g = sm.g[4 * lane + k];
                     unsigned long long s = 0ull;
                     if (anypos) {
                       if (rr[k] > 0.0) s = pack(f2key(__fadd_rn(logf((float)rr[k]), g)), (uint32_t)tok[k]);
