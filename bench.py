@@ -11,7 +11,8 @@ Gumbel sampling, accept test, residual and bonus tokens).
 
 Prints one JSON line (rank 0).  `value` is rows per second over all ranks,
 timed with CUDA events around K calls replayed from CUDA graphs with the
-inputs already resident in HBM; `e2e` is the same metric with each step's
+inputs already resident in HBM (the last G calls carry per-kernel events,
+which give the kernel durations of the roofline); `e2e` is the same metric with each step's
 inputs copied from pinned host memory and its tokens copied back inside the
 timed region.  Under torchrun each rank runs its own batch (weak scaling,
 no collective on the data path).  `--impl reference` times the CPU oracle.
@@ -289,13 +290,23 @@ def run_ours(args, w, desc):
         for i in range(2):
             run(logits=lg[i % 2], draft_probs=qq[i % 2])
     stream.synchronize()
+    # Two graphs of the same G calls: `graph` without instrumentation, and
+    # `graph_ev` with an event before, between and after the kernels of each
+    # call.  Event nodes cost about 15 us per call here, so the timed region
+    # replays `graph` for all but its last G calls, which come from `graph_ev`
+    # and give the per-kernel durations (measured inside the timed region).
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=stream):
+        for i in range(G):
+            run(logits=lg[i % 2], draft_probs=qq[i % 2])
+    graph_ev = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph_ev, stream=stream):
         for i in range(G):
             run(logits=lg[i % 2], draft_probs=qq[i % 2], events=ev[i])
     with torch.cuda.stream(stream):
         for _ in range(max(1, -(-Wm // G))):
             graph.replay()
+        graph_ev.replay()
     stream.synchronize()
 
     clocks = Clocks(local)
@@ -308,8 +319,9 @@ def run_ours(args, w, desc):
     t_end = torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         t_start.record(stream)
-        for _ in range(K // G):
+        for _ in range(K // G - 1):
             graph.replay()
+        graph_ev.replay()
         t_end.record(stream)
     torch.cuda.synchronize(dev)
     ck = clocks.stop()
@@ -378,7 +390,7 @@ def run_ours(args, w, desc):
             "config": {"workload": desc, "name": args.workload, "B": w.B, "V": w.V,
                        "positions": w.n_positions, "tile": tile, "tiles_per_row": run.plan.num_tiles,
                        "l2": "inputs larger than L2 (two resident copies alternated)",
-                       "graph": f"{G} calls per CUDA graph, {K // G} replays", "parallelism": f"replicas{world}"},
+                       "graph": f"{G} calls per CUDA graph, {K // G} replays, the last with per-kernel events", "parallelism": f"replicas{world}"},
             "roofline": {"bound": "hbm", "kernel": "stage1", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_kind": peak_kind,
                          "traffic": traffic, "alg_bytes_per_launch": alg1},
