@@ -47,6 +47,12 @@ def workload(name: str):
         "c3": (W.config3, "single-step top-k stress: B=256, V=262144 fp32, half near-flat rows"),
         "c4": (W.config4, "speculative verification: B=32, gamma=4, V=131072 bf16 target and draft probs"),
         "c1": (W.config1, "single-step: B=4, V=32000 fp32, 2 greedy + 2 stochastic rows"),
+        "c4_onehot": (lambda: W.with_one_hot_drafts(W.config4()),
+                      "speculative verification: B=32, gamma=4, V=131072 bf16 target, drafts without "
+                      "probabilities (one-hot q)"),
+        "c4_bounded": (lambda: W.with_bounded_p(W.config4()),
+                       "speculative verification: B=32, gamma=4, V=131072 bf16 target and draft probs, "
+                       "stochastic rows verified against the 128-candidate softmax"),
     }
     fn, desc = table[name]
     return fn(), desc
@@ -279,7 +285,7 @@ def run_ours(args, w, desc):
     K, Wm = args.steps, args.warmup
     # two resident copies of the large inputs, alternated between steps
     lg = [run.d["logits"], run.d["logits"].clone()]
-    qq = [run.d.get("draft_probs"), run.d["draft_probs"].clone() if verify else None]
+    qq = [run.d.get("draft_probs"), run.d["draft_probs"].clone() if "draft_probs" in run.d else None]
     G = max(d for d in range(1, min(10, K) + 1) if K % d == 0)
     stream = torch.cuda.Stream(device=dev)
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(G)]
@@ -415,7 +421,7 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="c5", choices=["c5", "c2", "c3", "c4", "c1"])
+    ap.add_argument("--workload", default="c5", choices=["c5", "c2", "c3", "c4", "c1", "c4_onehot", "c4_bounded"])
     ap.add_argument("--tile", type=int, default=0)
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-e2e", action="store_true")

@@ -85,7 +85,11 @@ enum {
   SS_BIAS = 1u << 3,     /* sparse logit bias */
   SS_TOPK = 1u << 4,     /* top_k > 0 keeps the top_k most probable */
   SS_TOPP = 1u << 5,     /* top_p < 1 keeps the nucleus */
-  SS_MINP = 1u << 6      /* min_p > 0 keeps p >= min_p * p_max */
+  SS_MINP = 1u << 6,     /* min_p > 0 keeps p >= min_p * p_max */
+  SS_BOUNDED_P = 1u << 7 /* verify: p is the softmax over the row's 128
+                            candidates even without truncation (no pass
+                            over the vocabulary; a draft outside them is
+                            rejected) */
 };
 
 /* Per-row status bits written to ss_out.row_status.  Data errors never trap. */
@@ -205,7 +209,13 @@ ss_status ss_sample(const void* logits, const ss_batch* params, const int32_t* h
  * target positions starting at cu_draft[r] + r; gamma_r = 0 is a single-step
  * row whose bonus token is its sample.
  * target_logits: [cu_draft[B] + B, ld_logits] (plan dtype).
- * draft_probs:   [cu_draft[B], ld_q] draft-model probabilities q (plan q dtype).
+ * draft_probs:   [cu_draft[B], ld_q] draft-model probabilities q (plan q dtype),
+ *                or NULL for drafts without probabilities (n-gram or
+ *                prompt-lookup drafts): q is then one-hot on the draft token,
+ *                so a draft is accepted iff u <= p(d) and a rejection samples
+ *                from p with the draft token removed (dl-note "Decoding and
+ *                sampling", Rejection Sampler, its example's no-draft-probs
+ *                case).  ld_q is ignored then.
  * draft_ids:     [cu_draft[B]] int32.
  * params:        as for ss_sample, plus cu_draft and the processor inputs
  *                history / bitmask (per target position) / bias.

@@ -40,8 +40,10 @@
 //    logit space, l_t - l_0 >= ln(min_p); the kept set is the shortest of the
 //    active prefixes (intersection), and at least one token;
 //  - verification: rows that request any truncation use the kept
-//    distribution as p; untruncated rows use the full-vocabulary softmax;
-//    greedy rows accept iff the draft equals the argmax.
+//    distribution as p; untruncated rows use the full-vocabulary softmax,
+//    unless flagged bounded-p (then the candidate softmax); greedy rows
+//    accept iff the draft equals the argmax.  Drafts without probabilities
+//    are given to the oracle as a one-hot q row (q(d) = 1).
 #include <algorithm>
 #include <cmath>
 #include <cstdint>
@@ -60,6 +62,7 @@ constexpr uint32_t kBias = 1u << 3;
 constexpr uint32_t kTopK = 1u << 4;
 constexpr uint32_t kTopP = 1u << 5;
 constexpr uint32_t kMinP = 1u << 6;
+constexpr uint32_t kBoundedP = 1u << 7;  // verify against the candidate distribution
 
 // Per-row status bits.
 constexpr uint32_t kStNan = 1u << 0;         // a processed logit was NaN -> -inf
@@ -200,6 +203,7 @@ bool row_truncates(const sso_row& rp) {
   if ((rp.flags & kTopK) && rp.top_k > 0) return true;
   if ((rp.flags & kTopP) && rp.top_p < 1.0f) return true;
   if ((rp.flags & kMinP) && rp.min_p > 0.0f) return true;
+  if (rp.flags & kBoundedP) return true;  // p = the kept (here: all finite) candidates
   return false;
 }
 

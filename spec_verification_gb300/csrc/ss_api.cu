@@ -330,17 +330,17 @@ ss_status ss_verify(const void* target_logits, const void* draft_probs, const in
   ss::Params P;
   ss_status s = fill_common(pl, params, target_logits, seeds, out, P);
   if (s != SS_OK) return s;
-  if (!params->cu_draft || !draft_ids || !draft_probs || !out->num_accepted)
-    return fail(SS_ERR_ARG, "cu_draft, draft_ids, draft_probs and num_accepted are required");
+  if (!params->cu_draft || !draft_ids || !out->num_accepted)
+    return fail(SS_ERR_ARG, "cu_draft, draft_ids and num_accepted are required");
   if (out->tokens_stride < 1) return fail(SS_ERR_ARG, "tokens_stride must be >= 1");
-  if (params->ld_q < pl->V) return fail(SS_ERR_ARG, "ld_q < V");
+  if (draft_probs && params->ld_q < pl->V) return fail(SS_ERR_ARG, "ld_q < V");
   P.cu_draft = params->cu_draft;
   P.history = params->history;
   P.bitmask = params->bitmask;
   P.bias = params->bias;
   P.draft_ids = draft_ids;
-  P.q = draft_probs;
-  P.ld_q = params->ld_q;
+  P.q = draft_probs;  // NULL: one-hot drafts
+  P.ld_q = draft_probs ? params->ld_q : 0;
   P.q_bf16 = pl->qdt == SS_BF16;
   P.mask_tma = mask_rows_copyable(P);
   DeviceGuard guard(pl->device);

@@ -164,8 +164,10 @@ __device__ __forceinline__ RowCtx make_row(const ss_row_params& p, int hist_stri
   }
   c.valid = ok;
   c.rT = c.stoch ? __fdiv_rn(1.0f, p.temperature) : 1.0f;
+  // truncating rows (and SS_BOUNDED_P rows) verify against the kept candidate
+  // distribution; the others against the softmax over the whole vocabulary
   c.trunc = c.stoch && (((p.flags & SS_TOPK) && p.top_k > 0) || ((p.flags & SS_TOPP) && p.top_p < 1.0f) ||
-                        ((p.flags & SS_MINP) && p.min_p > 0.0f));
+                        ((p.flags & SS_MINP) && p.min_p > 0.0f) || (p.flags & SS_BOUNDED_P));
   return c;
 }
 

@@ -103,6 +103,7 @@ __global__ void __launch_bounds__(kNT, 4) residual_kernel(const Params P) {
     const uint64_t seed = P.seeds[r];
     const float lse = (float)__ldcg(&P.ws.pos[pos].lse);
     const int64_t qrow = (int64_t)__ldg(P.cu_draft + r) + j;
+    const int32_t dtok = P.q ? -1 : __ldg(P.draft_ids + qrow);  // one-hot drafts: q = [i == dtok]
     const bool pen_on = (rc.flags & SS_PENALTY) && P.history != nullptr;
     const bool bias_on = (rc.flags & SS_BIAS) && P.bias != nullptr;
     const bool aux_on = pen_on || bias_on;
@@ -124,7 +125,7 @@ __global__ void __launch_bounds__(kNT, 4) residual_kernel(const Params P) {
         rr[k] = -1.0f;
         if (x[k] > -INFINITY && i0 + k < t0 + nt) {
           const float p = expf(x[k] - lse);
-          rr[k] = p - load_scalar(P.q, P.q_bf16, qrow * P.ld_q + i0 + k);
+          rr[k] = p - (P.q ? load_scalar(P.q, P.q_bf16, qrow * P.ld_q + i0 + k) : (i0 + k == dtok ? 1.0f : 0.0f));
           any |= rr[k] > 0.0f;
         }
       }

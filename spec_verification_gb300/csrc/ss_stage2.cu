@@ -137,7 +137,7 @@ __global__ void __launch_bounds__(kNT2, 9) stage2_kernel(const Params P, int ver
         float qd = 0.0f;
         if (verify && j < gamma) {
           d = __ldg(P.draft_ids + c0 + j);
-          if (d >= 0 && d < V) qd = load_scalar(P.q, P.q_bf16, ((int64_t)c0 + j) * P.ld_q + d);
+          if (d >= 0 && d < V) qd = P.q ? load_scalar(P.q, P.q_bf16, ((int64_t)c0 + j) * P.ld_q + d) : 1.0f;
         }
         sm.d = d;
         sm.qd = qd;
@@ -413,7 +413,8 @@ __global__ void __launch_bounds__(kNT2, 9) stage2_kernel(const Params P, int ver
                 for (int k = 0; k < 4; ++k) {
                   rr[k] = 0.0;
                   if (4 * lane + k < nk)
-                    rr[k] = fmax(0.0, w[k] * izk - (double)load_scalar(P.q, P.q_bf16, qrow * P.ld_q + tok[k]));
+                    rr[k] = fmax(0.0, w[k] * izk - (P.q ? (double)load_scalar(P.q, P.q_bf16, qrow * P.ld_q + tok[k])
+                                                        : (tok[k] == d ? 1.0 : 0.0)));
                   pos_any |= (4 * lane + k < nk && rr[k] > 0.0);
                 }
                 const bool anypos = __any_sync(0xffffffffu, pos_any);

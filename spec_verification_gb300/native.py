@@ -202,7 +202,8 @@ def ss_verify(plan: Plan, target_logits, draft_probs, draft_ids, rows, cu_draft,
     b = Batch()
     b.B = B if B is not None else seeds.shape[0]
     b.ld_logits = target_logits.stride(0)
-    b.ld_q = draft_probs.stride(0) if draft_probs.dim() == 2 else plan.V
+    # draft_probs None: drafts without probabilities (q one-hot on the draft token)
+    b.ld_q = plan.V if draft_probs is None or draft_probs.dim() != 2 else draft_probs.stride(0)
     b.rows = _ptr(rows)
     b.cu_draft = _ptr(cu_draft)
     b.hist_stride, b.bias_stride = hist_stride, bias_stride

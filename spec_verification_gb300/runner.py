@@ -60,11 +60,14 @@ class DeviceRun:
     """Inputs, outputs and workspace of one call, resident on one GPU."""
 
     def __init__(self, w: Workload, device: str = "cuda:0", tile: int = 0, max_positions: int | None = None,
-                 candidates: bool = True, tokens_stride: int | None = None, pinned_host: bool = False):
+                 candidates: bool = True, tokens_stride: int | None = None, pinned_host: bool = False,
+                 one_hot_drafts: bool = False):
         import torch
         self.w = w
         self.dev = torch.device(device)
         self.verify = w.is_verify
+        # drafts without probabilities: nothing of q is uploaded; the library gets NULL
+        self.one_hot_drafts = self.verify and (one_hot_drafts or bool(w.meta.get("one_hot_drafts")))
         npos = w.n_positions
         self.plan = native.Plan(w.V, w.B, max_positions or npos, w.dtype,
                                 w.q_dtype if self.verify else "f32", tile, self.dev.index or 0)
@@ -80,13 +83,14 @@ class DeviceRun:
         if self.verify:
             host["cu_draft"] = _as_torch_bits(w.cu_draft.astype(np.int32))
             host["draft_ids"] = _as_torch_bits(w.draft_ids.astype(np.int32))
-            host["draft_probs"] = _as_torch_bits(_padded_rows(w.draft_probs, 2 if w.q_dtype == "bf16" else 4))
+            if not self.one_hot_drafts:
+                host["draft_probs"] = _as_torch_bits(_padded_rows(w.draft_probs, 2 if w.q_dtype == "bf16" else 4))
         if pinned_host:
             host = {k: v.pin_memory() for k, v in host.items()}
         self.host = host
         self.d = {k: v.to(self.dev) for k, v in host.items()}
         self.ld_logits = int(self.host["logits"].shape[1])
-        self.ld_q = int(self.host["draft_probs"].shape[1]) if self.verify else 0
+        self.ld_q = int(self.host["draft_probs"].shape[1]) if "draft_probs" in self.host else 0
         self.hist_stride = int(w.history.shape[1])
         self.bias_stride = int(w.bias_tokens.shape[1])
         i32 = torch.int32
@@ -123,7 +127,7 @@ class DeviceRun:
         d = self.d
         lg = logits if logits is not None else d["logits"]
         if self.verify:
-            q = draft_probs if draft_probs is not None else d["draft_probs"]
+            q = None if self.one_hot_drafts else (draft_probs if draft_probs is not None else d["draft_probs"])
             native.ss_verify(self.plan, lg, q, d["draft_ids"], d["rows"], d["cu_draft"], d["seeds"],
                              workspace=self.workspace, tokens=self.tokens, num_accepted=self.num_accepted,
                              row_status=self.row_status, history=d["history"], bitmask=d.get("bitmask"),

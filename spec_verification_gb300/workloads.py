@@ -40,6 +40,7 @@ BIAS = 1 << 3
 TOPK = 1 << 4
 TOPP = 1 << 5
 MINP = 1 << 6
+BOUNDED_P = 1 << 7   # verify against the candidate softmax even without truncation
 
 ROW_FIELDS = ("flags", "temperature", "top_p", "min_p", "rep", "freq", "pres",
               "top_k", "hist_len", "n_bias", "position")
@@ -106,7 +107,7 @@ class Workload:
         n = self.logits.nbytes
         if self.bitmask is not None:
             n += self.bitmask.nbytes
-        if self.draft_probs is not None:
+        if self.draft_probs is not None and not self.meta.get("one_hot_drafts"):
             n += self.draft_probs.nbytes
         n += 2 * self.n_positions * z * 128 * 8
         return n
@@ -449,6 +450,27 @@ def subset(w, rows) -> Workload:
                     None if w.bitmask is None else w.bitmask[pos], w.bias_tokens[rows], w.bias_values[rows],
                     w.seeds[rows], cu_draft=cu, draft_ids=w.draft_ids[qr], draft_probs=w.draft_probs[qr],
                     q_dtype=w.q_dtype, meta=meta)
+
+
+def with_one_hot_drafts(w: Workload) -> Workload:
+    """The same verify batch with drafts that carry no probabilities: the
+    library is called with draft_probs = NULL (meta["one_hot_drafts"]), and
+    draft_probs holds the equivalent one-hot q rows for the oracle."""
+    d = np.asarray(w.draft_ids, np.int64)
+    q = np.zeros((d.size, w.V), np.float32)
+    q[np.arange(d.size), d] = 1.0
+    w.draft_probs = f32_to_bf16_bits(q) if w.q_dtype == "bf16" else q
+    w.meta = dict(w.meta, one_hot_drafts=True)
+    w.name = w.name + "_onehot"
+    return w
+
+
+def with_bounded_p(w: Workload) -> Workload:
+    """The same verify batch with every stochastic row flagged BOUNDED_P."""
+    stoch = (w.rows["flags"] & GREEDY) == 0
+    w.rows["flags"][stoch] |= np.uint32(BOUNDED_P)
+    w.name = w.name + "_bounded"
+    return w
 
 
 CONFIGS = {1: config1, 2: config2, 3: config3, 4: config4, 5: config5}

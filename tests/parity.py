@@ -26,7 +26,7 @@ GUMBEL_TOL = 1e-5
 PROB_TOL = 1e-5
 
 GREEDY = 1
-TOPK, TOPP, MINP = 16, 32, 64
+TOPK, TOPP, MINP, BOUNDED_P = 16, 32, 64, 128
 
 
 def _trunc(rows, r):
@@ -34,7 +34,7 @@ def _trunc(rows, r):
     if f & GREEDY:
         return False
     return bool(((f & TOPK) and rows["top_k"][r] > 0) or ((f & TOPP) and rows["top_p"][r] < 1)
-                or ((f & MINP) and rows["min_p"][r] > 0))
+                or ((f & MINP) and rows["min_p"][r] > 0) or (f & BOUNDED_P))
 
 
 class Report:

@@ -232,6 +232,36 @@ def test_verify_truncated_bf16(tile):
     check(w, tile=tile)
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_verify_one_hot_drafts(dtype):
+    # drafts without probabilities: the library gets draft_probs = NULL and the
+    # oracle the equivalent one-hot q; truncated, untruncated (residual passes
+    # over V with q one-hot) and greedy rows, processors on
+    w = W.verify_workload(34, 16, 40000, [1, 2, 3, 4, 0, 5, 6, 7, 2, 1, 3, 3, 2, 4, 1, 0], dtype, dtype,
+                          processors=True, truncation=True, noise=2.0)
+    d = w.draft_ids
+    q = np.zeros((d.size, w.V), np.float32)
+    q[np.arange(d.size), d] = 1.0
+    w.draft_probs = W.f32_to_bf16_bits(q) if dtype == "bf16" else q
+    # half of the stochastic rows without truncation, so that rejections there
+    # take the pass over the vocabulary
+    untr = (np.arange(w.B) % 2 == 0) & ((w.rows["flags"] & F.GREEDY) == 0)
+    w.rows["flags"][untr] &= ~np.uint32(F.TOPK | F.TOPP | F.MINP)
+    gpu, ora, dev = check(w, one_hot_drafts=True)
+    assert np.any(ora["num_accepted"] < np.diff(w.cu_draft))   # some rejections
+    assert dev.diag()[2] > 0                                    # residual passes with q one-hot
+
+
+def test_verify_bounded_p_rows():
+    # untruncated stochastic rows, half of them flagged SS_BOUNDED_P (candidate
+    # softmax, no pass over the vocabulary)
+    w = W.verify_workload(35, 12, 30000, np.full(12, 3), "bf16", "bf16", noise=3.0)
+    stoch = (w.rows["flags"] & F.GREEDY) == 0
+    w.rows["flags"][stoch & (np.arange(w.B) % 2 == 1)] |= np.uint32(F.BOUNDED_P)
+    gpu, ora, dev = check(w)
+    assert np.any(ora["num_accepted"][stoch] < 3)
+
+
 def test_verify_edge_cases():
     rng = np.random.default_rng(34)
     V = 9000

@@ -443,6 +443,78 @@ def test_verify_output_distributed_as_p(trunc):
     assert abs(acc - want) < 4 * np.sqrt(want * (1 - want) / B) + 1e-3
 
 
+def _one_hot(d, V):
+    q = np.zeros((len(d), V), np.float32)
+    q[np.arange(len(d)), d] = 1.0
+    return q
+
+
+@pytest.mark.parametrize("trunc", [False, True])
+def test_verify_one_hot_drafts_distributed_as_p(trunc):
+    """Drafts without probabilities (dl-note, Rejection Sampler, the case
+    without draft probabilities): q is one-hot on the draft d, so d is kept
+    with probability p(d) and a rejection draws from p without d.  Whatever
+    distribution the drafts come from, the output is distributed as p and the
+    acceptance rate is E[p(d)]."""
+    rng = np.random.default_rng(41 + trunc)
+    V, B = 20, 40000
+    pl = (rng.standard_normal(V) * 1.5).astype(np.float32)
+    flags = (F.TOPK | F.TOPP) if trunc else 0
+    d = rng.integers(0, V, B).astype(np.int32)           # drafts from an unrelated proposal
+    tgt = np.repeat(pl[None], 2 * B, 0)
+    w = verify_case(tgt, _one_hot(d, V), d, np.ones(B), flags=flags, top_k=10, top_p=0.95,
+                    seeds=np.arange(B, dtype=np.uint64) * 7727 + 11)
+    out = O.verify(w)
+    if trunc:
+        s = O.sample(sample_case(pl[None], flags=flags, top_k=10, top_p=0.95))
+        n = int(s["num_kept"][0])
+        p = np.zeros(V)
+        p[s["cand_ids"][0, :n]] = s["cand_probs"][0, :n]
+    else:
+        p = _softmax64(pl)
+    counts = np.bincount(out["tokens"][:, 0], minlength=V)
+    assert chi2_pvalue(counts, p) > 1e-4
+    acc = out["num_accepted"].mean()
+    want = p[d].mean()
+    assert abs(acc - want) < 4 * np.sqrt(want * (1 - want) / B) + 1e-3
+    # a rejection never returns the rejected draft
+    rej = out["num_accepted"] == 0
+    assert not np.any(out["tokens"][rej, 0] == d[rej])
+
+
+def test_bounded_p_rejects_drafts_outside_the_candidates():
+    """SS_BOUNDED_P: p is the softmax over the 128 candidates.  With 300 equal
+    logits the candidates are tokens 0..127 (ties go to the lower index); a
+    draft 200 with q = uniform is always kept under the full-vocabulary p
+    (u q(d) <= p(d) = q(d)) and never under the bounded p (p(d) = 0)."""
+    V, B = 300, 64
+    tgt = np.zeros((2 * B, V), np.float32)
+    q = np.full((B, V), 1.0 / V, np.float32)
+    d = np.full(B, 200, np.int32)
+    flags = np.where(np.arange(B) % 2 == 1, F.BOUNDED_P, 0).astype(np.uint32)
+    w = verify_case(tgt, q, d, np.ones(B), flags=0, seeds=np.arange(B, dtype=np.uint64) + 1)
+    w.rows["flags"][:] = flags
+    out = O.verify(w)
+    assert np.all(out["num_accepted"][0::2] == 1)
+    assert np.all(out["num_accepted"][1::2] == 0)
+    assert np.all(out["tokens"][1::2, 0] < 128)        # resampled among the candidates
+
+
+def test_bounded_p_is_the_full_p_when_v_is_at_most_128():
+    """With V <= 128 the candidates are the whole vocabulary, so the flag
+    changes nothing."""
+    rng = np.random.default_rng(43)
+    V, B = 96, 3000
+    pl = (rng.standard_normal(V) * 2).astype(np.float32)
+    q = _softmax64((rng.standard_normal(V) * 2).astype(np.float32))
+    w = _verify_stat_case(V, B, pl, q, 2, 0, 17)
+    a = O.verify(w)
+    w.rows["flags"][:] = F.BOUNDED_P
+    b = O.verify(w)
+    np.testing.assert_array_equal(a["tokens"], b["tokens"])
+    np.testing.assert_array_equal(a["num_accepted"], b["num_accepted"])
+
+
 def test_golden_rejection_closed_forms():
     fx = json.load(open(os.path.join(GOLDEN, "rejection_examples.json")))[0]
     p = np.array(fx["p"])
