@@ -486,6 +486,15 @@ __device__ __forceinline__ float stream_value(const unsigned char* ring, const u
   return __fmul_rn(v, rT);
 }
 
+// 2^x by the hardware approximation (PTX ex2.approx, relative error about
+// 2^-22): the normaliser partials feed only the full-vocabulary acceptance
+// test, whose stated tolerance is 1e-5 relative.  ex2(-inf) = +0.
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Running (max, sum exp(x - max)) of one thread; -inf (and NaN) terms add nothing.
 __device__ __forceinline__ void lse_add(float& M, float& S, float v) {
   if (!(v > -INFINITY)) return;
@@ -869,11 +878,12 @@ __global__ void __launch_bounds__(kNT, 2) stage1_kernel(const Params P) {
               if (mc > -INFINITY) {
                 const float Mn = fmaxf(lM, mc);
                 const float off = Mn * kLog2e;
-                float s = 0.0f;
+                // four independent sums; fmaxf(NaN, -inf) = -inf drops NaN terms
+                float s4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
                 for (int e = 0; e < kPT; ++e)
-                  if (x[e] > -INFINITY) s += exp2f(__fmaf_rn(x[e], kLog2e, -off));
-                lS = lS * exp2f((lM - Mn) * kLog2e) + s;
+                  s4[e & 3] += ex2_approx(__fmaf_rn(fmaxf(x[e], -INFINITY), kLog2e, -off));
+                lS = lS * ex2_approx((lM - Mn) * kLog2e) + ((s4[0] + s4[1]) + (s4[2] + s4[3]));
                 lM = Mn;
               }
             }
