@@ -868,12 +868,25 @@ __global__ void __launch_bounds__(kNT, 2) stage1_kernel(const Params P) {
               }
             }
             if (lse_on) {
-              float mc = -INFINITY;
+              // the chunk's maximum without NaN: load_chunk's (NaN-propagating)
+              // maximum unless a NaN or a count-table row needs it recomputed
+              float mc = m;
+              if (staged || mc != mc) {
+                if (staged) {
 #pragma unroll
-              for (int e = 0; e < kPT; ++e) {
-                const int li = elem_index<VEC>(ch, e / VEC, e % VEC);
-                if (staged && (full || li < nt) && aux[li] != 0u) x[e] = -INFINITY;  // added with its exact value
-                mc = fmaxf(mc, x[e]);
+                  for (int e = 0; e < kPT; ++e) {
+                    const int li = elem_index<VEC>(ch, e / VEC, e % VEC);
+                    if ((full || li < nt) && aux[li] != 0u) x[e] = -INFINITY;  // added with its exact value
+                  }
+                }
+                float t[kPT / 2];
+#pragma unroll
+                for (int e = 0; e < kPT / 2; ++e) t[e] = fmaxf(x[2 * e], x[2 * e + 1]);
+#pragma unroll
+                for (int w = kPT / 4; w >= 1; w >>= 1)
+#pragma unroll
+                  for (int e = 0; e < w; ++e) t[e] = fmaxf(t[e], t[e + w]);
+                mc = t[0];
               }
               if (mc > -INFINITY) {
                 const float Mn = fmaxf(lM, mc);
