@@ -50,6 +50,9 @@ def workload(name: str):
         "c4_onehot": (lambda: W.with_one_hot_drafts(W.config4()),
                       "speculative verification: B=32, gamma=4, V=131072 bf16 target, drafts without "
                       "probabilities (one-hot q)"),
+        "c2_exact": (lambda: W.with_exact_sampling(W.config2()),
+                     "single-step heterogeneous: B=64, V=131072 bf16, all processors, stochastic rows "
+                     "untruncated and sampled over the whole vocabulary (exact sampling)"),
         "c4_bounded": (lambda: W.with_bounded_p(W.config4()),
                        "speculative verification: B=32, gamma=4, V=131072 bf16 target and draft probs, "
                        "stochastic rows verified against the 128-candidate softmax"),
@@ -421,7 +424,7 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="c5", choices=["c5", "c2", "c3", "c4", "c1", "c4_onehot", "c4_bounded"])
+    ap.add_argument("--workload", default="c5", choices=["c5", "c2", "c3", "c4", "c1", "c4_onehot", "c4_bounded", "c2_exact"])
     ap.add_argument("--tile", type=int, default=0)
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-e2e", action="store_true")

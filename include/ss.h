@@ -86,10 +86,15 @@ enum {
   SS_TOPK = 1u << 4,     /* top_k > 0 keeps the top_k most probable */
   SS_TOPP = 1u << 5,     /* top_p < 1 keeps the nucleus */
   SS_MINP = 1u << 6,     /* min_p > 0 keeps p >= min_p * p_max */
-  SS_BOUNDED_P = 1u << 7 /* verify: p is the softmax over the row's 128
-                            candidates even without truncation (no pass
-                            over the vocabulary; a draft outside them is
-                            rejected) */
+  SS_BOUNDED_P = 1u << 7, /* verify: p is the softmax over the row's 128
+                             candidates even without truncation (no pass
+                             over the vocabulary; a draft outside them is
+                             rejected) */
+  SS_EXACT = 1u << 8      /* untruncated stochastic rows: the sample (and
+                             the bonus token of a verify row) is the
+                             Gumbel-max over the whole vocabulary, not over
+                             the 128 candidates (exact softmax sampling);
+                             needs a plan with ss_plan_enable_exact */
 };
 
 /* Per-row status bits written to ss_out.row_status.  Data errors never trap. */
@@ -101,7 +106,9 @@ enum {
   SS_ST_BAD_PARAM = 1u << 4,   /* invalid parameters: no tokens (-1) */
   SS_ST_BAD_DRAFT = 1u << 5,   /* a draft id outside [0, V): rejected */
   SS_ST_POS_INF = 1u << 6,     /* +inf processed logit: point mass on it */
-  SS_ST_RESID_EMPTY = 1u << 7  /* residual max(0, p - q) had no mass: sampled from p */
+  SS_ST_RESID_EMPTY = 1u << 7, /* residual max(0, p - q) had no mass: sampled from p */
+  SS_ST_NOT_EXACT = 1u << 8     /* SS_EXACT on a plan without exact sampling:
+                                   sampled from the 128 candidates */
 };
 
 /* One row's sampling parameters (device array of B entries, 44 bytes each).
@@ -189,6 +196,19 @@ int32_t ss_plan_num_tiles(const ss_plan* plan);
  * min(this, B_pos * Z_v) contiguous runs, one per CTA; a run's part inside
  * one position is a segment, which leaves one list of 128 candidates. */
 int32_t ss_plan_stage1_ctas(const ss_plan* plan);
+
+/* Exact sampling for rows flagged SS_EXACT (an addition of this library,
+ * following the pages' note that a tile-local Gumbel-max is exact and
+ * decomposes over tiles): enable != 0 makes the plan run the stage-1 variant
+ * that also keeps, per segment, the Gumbel-max of l_i + g_i over every token
+ * (g_i the Philox purpose-0 noise of the sampler); stage 2 then takes the
+ * largest of a position's segment maxima as the token.  Off by default: the
+ * default variant's streaming loop carries none of this work.  On a plan
+ * without it, SS_EXACT rows are sampled from their 128 candidates and report
+ * SS_ST_NOT_EXACT.  Not thread-safe against calls using the plan.
+ * Returns SS_ERR_ARG for a NULL plan, SS_ERR_CUDA if the kernel cannot be
+ * configured. */
+ss_status ss_plan_enable_exact(ss_plan* plan, int enable);
 
 /* Single-step sampling (SonicSampler 3.1-3.2; dl-note Combination).
  * logits:  [B, ld_logits] fp32 or bf16 (plan dtype), rows 16-byte aligned.

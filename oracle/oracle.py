@@ -57,7 +57,7 @@ class Problem(C.Structure):
                 ("bias_values", C.c_void_p), ("bias_stride", C.c_int32),
                 ("seeds", C.c_void_p), ("cu_draft", C.c_void_p), ("draft_ids", C.c_void_p),
                 ("q_bf16", C.c_int32), ("ld_q", C.c_int64), ("draft_probs", C.c_void_p),
-                ("row_ids", C.c_void_p)]
+                ("row_ids", C.c_void_p), ("exact_on", C.c_int32)]
 
 
 class Outputs(C.Structure):
@@ -128,6 +128,7 @@ def _problem(w, keep: list, rows_override=None):
         P.q_bf16 = 1 if w.q_dtype == "bf16" else 0
         P.ld_q = q.shape[1] if q.ndim == 2 and q.shape[0] else w.V
         P.draft_probs = _ptr(q)
+    P.exact_on = 1 if (getattr(w, "meta", None) or {}).get("exact_sampling") else 0
     rid = getattr(w, "meta", {}).get("row_ids") if hasattr(w, "meta") else None
     if rid is not None:
         rid = np.ascontiguousarray(np.asarray(rid, np.int32))

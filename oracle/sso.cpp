@@ -43,7 +43,9 @@
 //    distribution as p; untruncated rows use the full-vocabulary softmax,
 //    unless flagged bounded-p (then the candidate softmax); greedy rows
 //    accept iff the draft equals the argmax.  Drafts without probabilities
-//    are given to the oracle as a one-hot q row (q(d) = 1).
+//    are given to the oracle as a one-hot q row (q(d) = 1);
+//  - rows flagged exact (untruncated, stochastic) sample by the Gumbel-max
+//    over every finite token of the vocabulary instead of the candidates.
 #include <algorithm>
 #include <cmath>
 #include <cstdint>
@@ -63,6 +65,7 @@ constexpr uint32_t kTopK = 1u << 4;
 constexpr uint32_t kTopP = 1u << 5;
 constexpr uint32_t kMinP = 1u << 6;
 constexpr uint32_t kBoundedP = 1u << 7;  // verify against the candidate distribution
+constexpr uint32_t kExact = 1u << 8;     // sample over the whole vocabulary
 
 // Per-row status bits.
 constexpr uint32_t kStNan = 1u << 0;         // a processed logit was NaN -> -inf
@@ -73,6 +76,7 @@ constexpr uint32_t kStBadParam = 1u << 4;    // invalid parameters -> no tokens
 constexpr uint32_t kStBadDraft = 1u << 5;    // draft id outside [0, V) -> rejected
 constexpr uint32_t kStPosInf = 1u << 6;      // +inf processed logit -> point mass
 constexpr uint32_t kStResidEmpty = 1u << 7;  // residual had no mass -> sampled from p
+constexpr uint32_t kStNotExact = 1u << 8;    // SS_EXACT without exact sampling -> candidates
 
 constexpr int kK = 128;  // bounded candidate count ([SS] 1, 3.3)
 constexpr float kNegInf = -std::numeric_limits<float>::infinity();
@@ -110,6 +114,7 @@ struct sso_problem {
   int64_t ld_q;
   const void* draft_probs;    // [cu_draft[B], ld_q]
   const int32_t* row_ids;     // [B] batch row index used in the Philox counter, or null (= r)
+  int32_t exact_on;           // SS_EXACT rows sample over the vocabulary (else: candidates + status)
 };
 
 struct sso_outputs {
@@ -198,11 +203,18 @@ bool row_params_valid(const sso_row& rp, const sso_problem& P) {
   return true;
 }
 
-bool row_truncates(const sso_row& rp) {
+// A stochastic row that asks for top-k, top-p or min-p.
+bool row_cuts(const sso_row& rp) {
   if (rp.flags & kGreedy) return false;
   if ((rp.flags & kTopK) && rp.top_k > 0) return true;
   if ((rp.flags & kTopP) && rp.top_p < 1.0f) return true;
   if ((rp.flags & kMinP) && rp.min_p > 0.0f) return true;
+  return false;
+}
+
+bool row_truncates(const sso_row& rp) {
+  if (rp.flags & kGreedy) return false;
+  if (row_cuts(rp)) return true;
   if (rp.flags & kBoundedP) return true;  // p = the kept (here: all finite) candidates
   return false;
 }
@@ -437,9 +449,18 @@ Pick sample_position(const sso_problem& P, int r, uint32_t position, const PosRe
   if (R.d.no_finite) { *status |= kStNoFinite; return p; }
   if (R.d.pos_inf) { *status |= kStPosInf; p.token = R.ord[0]; return p; }
   if (P.rows[r].flags & kGreedy) { p.token = R.ord[0]; return p; }
-  std::vector<int32_t> ids(R.ord.begin(), R.ord.begin() + R.d.n);
-  std::vector<float> base(R.d.n);
-  for (int t = 0; t < R.d.n; ++t) base[t] = R.x[R.ord[t]];
+  std::vector<int32_t> ids;
+  std::vector<float> base;
+  const bool exact_row = (P.rows[r].flags & kExact) && !row_cuts(P.rows[r]);
+  if (exact_row && !P.exact_on) *status |= kStNotExact;
+  if (exact_row && P.exact_on) {
+    // exact sampling: the Gumbel-max over every finite token of the vocabulary
+    for (int32_t i = 0; i < (int32_t)R.x.size(); ++i)
+      if (R.x[i] > -std::numeric_limits<float>::infinity()) { ids.push_back(i); base.push_back(R.x[i]); }
+  } else {
+    ids.assign(R.ord.begin(), R.ord.begin() + R.d.n);
+    for (int t = 0; t < R.d.n; ++t) base.push_back(R.x[R.ord[t]]);
+  }
   return gumbel_argmax(ids, base, P.seeds[r], position, philox_row(P, r), kPurposeSample);
 }
 

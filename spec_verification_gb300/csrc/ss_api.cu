@@ -13,8 +13,8 @@
 #include "ss_common.cuh"
 
 namespace ss {
-const void* stage1_ptr(bool bf16);
-void stage1_launch(bool bf16, int grid, size_t smem, cudaStream_t st, const Params& P);
+const void* stage1_ptr(bool bf16, bool exact);
+void stage1_launch(bool bf16, bool exact, int grid, size_t smem, cudaStream_t st, const Params& P);
 __global__ void stage2_kernel(const Params P, int verify);
 __global__ void residual_kernel(const Params P);
 size_t stage1_smem_bytes(int BN, bool bf16, int nslot);
@@ -27,12 +27,13 @@ int residual_piece_tokens();
 
 struct ss_plan {
   int V, max_rows, max_positions, BN, Z, device, sms, nslot;
+  int exact;  // stage 1 runs its exact-sampling variant
   ss_dtype ldt, qdt;
   int grid1, grid2, grid3;
   std::vector<int> grid2_by_cap;  // stage-2 grid for a shared-memory capacity of c lists (index c)
   size_t smem1, smem2, smem3;
   const void* k1;
-  size_t off_staging, off_tlse, off_tst, off_pos, off_rowc, off_rescnt, off_res, off_diag, ws_bytes;
+  size_t off_staging, off_tlse, off_tgm, off_tst, off_pos, off_rowc, off_rescnt, off_res, off_diag, ws_bytes;
 };
 
 namespace {
@@ -135,7 +136,8 @@ ss_status ss_plan_create(ss_plan** out, int32_t V, int32_t max_rows, int32_t max
   p->nslot = nslot;
   p->ldt = logits_dtype;
   p->qdt = q_dtype;
-  p->k1 = ss::stage1_ptr(bf16);
+  p->k1 = ss::stage1_ptr(bf16, false);
+  p->exact = 0;
   p->smem1 = ss::stage1_smem_bytes(BN, bf16, nslot);
   p->smem2 = ss::stage2_smem_bytes(p->Z);
   p->smem3 = ss::residual_smem_bytes(BN);
@@ -184,6 +186,7 @@ ss_status ss_plan_create(ss_plan** out, int32_t V, int32_t max_rows, int32_t max
   const size_t P = (size_t)max_positions, R = (size_t)max_rows, PZ = P * p->Z;
   p->off_staging = off; off = align_up(off + PZ * ss::kK * 8, 256);
   p->off_tlse = off;    off = align_up(off + PZ * 8, 256);
+  p->off_tgm = off;     off = align_up(off + PZ * 8, 256);
   p->off_tst = off;     off = align_up(off + PZ * 4, 256);
   p->off_pos = off;     off = align_up(off + P * sizeof(ss::PosResult), 256);
   p->off_rowc = off;    off = align_up(off + R * 4, 256);
@@ -201,6 +204,20 @@ size_t ss_workspace_bytes(const ss_plan* p) { return p ? p->ws_bytes : 0; }
 int32_t ss_plan_tile(const ss_plan* p) { return p ? p->BN : 0; }
 int32_t ss_plan_num_tiles(const ss_plan* p) { return p ? p->Z : 0; }
 int32_t ss_plan_stage1_ctas(const ss_plan* p) { return p ? p->grid1 : 0; }
+
+ss_status ss_plan_enable_exact(ss_plan* p, int enable) {
+  if (!p) return fail(SS_ERR_ARG, "plan is required");
+  if (enable) {
+    DeviceGuard guard(p->device);
+    // same launch bounds and shared memory as the default variant, so the
+    // occupancy (and with it the stage-1 split) does not change
+    const cudaError_t e = cudaFuncSetAttribute(ss::stage1_ptr(p->ldt == SS_BF16, true),
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p->smem1);
+    if (e != cudaSuccess) return cuda_fail(e, "kernel attributes");
+  }
+  p->exact = enable ? 1 : 0;
+  return SS_OK;
+}
 size_t ss_workspace_diag_offset(const ss_plan* p) { return p ? p->off_diag : 0; }
 
 }  // extern "C"
@@ -241,6 +258,7 @@ ss_status fill_common(const ss_plan* pl, const ss_batch* b, const void* logits, 
   char* w = static_cast<char*>(b->workspace);
   P.ws.staging = reinterpret_cast<unsigned long long*>(w + pl->off_staging);
   P.ws.tile_lse = reinterpret_cast<float2*>(w + pl->off_tlse);
+  P.ws.tile_gmax = reinterpret_cast<unsigned long long*>(w + pl->off_tgm);
   P.ws.tile_status = reinterpret_cast<uint32_t*>(w + pl->off_tst);
   P.ws.pos = reinterpret_cast<ss::PosResult*>(w + pl->off_pos);
   P.ws.row_count = reinterpret_cast<uint32_t*>(w + pl->off_rowc);
@@ -273,6 +291,7 @@ int seg_cap_for(const ss_plan* pl, int B) {
 ss_status launch(const ss_plan* pl, const ss::Params& P0, cudaStream_t st, bool verify, void* const* ev) {
   ss::Params P = P0;
   P.seg_cap = seg_cap_for(pl, P.B);
+  P.exact_on = pl->exact;
   const size_t smem2 = ss::stage2_smem_bytes(P.seg_cap);
   const int grid2 = pl->grid2_by_cap[P.seg_cap];
   cudaError_t e = cudaSuccess;
@@ -289,7 +308,7 @@ ss_status launch(const ss_plan* pl, const ss::Params& P0, cudaStream_t st, bool 
       e = cudaEventRecordWithFlags(static_cast<cudaEvent_t>(ev[i]), st, rec_flags);
   };
   rec(0);
-  ss::stage1_launch(pl->ldt == SS_BF16, pl->grid1, pl->smem1, st, P);
+  ss::stage1_launch(pl->ldt == SS_BF16, pl->exact != 0, pl->grid1, pl->smem1, st, P);
   rec(1);
   ss::stage2_kernel<<<grid2, ss::stage2_threads(), smem2, st>>>(P, verify ? 1 : 0);
   rec(2);

@@ -37,6 +37,7 @@ struct ResidEntry {
 struct Workspace {
   unsigned long long* staging;   // [P * Z * 128] packed candidates, one list per segment
   float2* tile_lse;              // [P * Z] per segment (max, sum exp(x - max)) when requested
+  unsigned long long* tile_gmax; // [P * Z] per segment Gumbel-max (key(l + g) << 32 | ~token) when requested
   uint32_t* tile_status;         // [P * Z] per segment SS_ST_* bits
   PosResult* pos;                // [P]
   uint32_t* row_count;           // [R] positions of the row done (stage-2 arrivals)
@@ -69,6 +70,7 @@ struct Params {
   int grid1;                // CTAs of the stage-1 launch (fixes the segment split)
   int nslot;                // stage-1 ring slots
   int seg_cap;              // segment lists per position that stage 2's shared memory holds
+  int exact_on;             // the plan runs the exact-sampling variant of stage 1
   int mask_tma;             // bitmask rows can be bulk-copied (16-byte aligned rows)
   Workspace ws;
   ss_out out;
@@ -137,6 +139,7 @@ struct RowCtx {
   int top_k, hist_len, n_bias;
   uint32_t position;
   bool valid, stoch, trunc;
+  bool exact;  // SS_EXACT on an untruncated stochastic row: sample over the whole vocabulary
 };
 
 __device__ __forceinline__ bool finitef(float x) { return fabsf(x) <= 3.402823466e38f; }
@@ -166,8 +169,10 @@ __device__ __forceinline__ RowCtx make_row(const ss_row_params& p, int hist_stri
   c.rT = c.stoch ? __fdiv_rn(1.0f, p.temperature) : 1.0f;
   // truncating rows (and SS_BOUNDED_P rows) verify against the kept candidate
   // distribution; the others against the softmax over the whole vocabulary
-  c.trunc = c.stoch && (((p.flags & SS_TOPK) && p.top_k > 0) || ((p.flags & SS_TOPP) && p.top_p < 1.0f) ||
-                        ((p.flags & SS_MINP) && p.min_p > 0.0f) || (p.flags & SS_BOUNDED_P));
+  const bool cuts = ((p.flags & SS_TOPK) && p.top_k > 0) || ((p.flags & SS_TOPP) && p.top_p < 1.0f) ||
+                   ((p.flags & SS_MINP) && p.min_p > 0.0f);
+  c.trunc = c.stoch && (cuts || (p.flags & SS_BOUNDED_P));
+  c.exact = c.stoch && !cuts && (p.flags & SS_EXACT);
   return c;
 }
 

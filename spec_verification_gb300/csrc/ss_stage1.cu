@@ -91,6 +91,7 @@ struct __align__(16) S1Smem {
   int dead, nan_flag, nf, out_cnt;
   uint32_t rowbad;  // SS_ST_BAD_HIST / SS_ST_BAD_BIAS of the segment's row
   int pad2[3];
+  unsigned long long gmax;  // the segment's Gumbel-max so far (exact sampling)
 };
 
 struct Layout {
@@ -495,6 +496,46 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// Exact sampling: this thread's Gumbel-max of l_i + g_i over chunk ch, the
+// processed values recomputed from the slot (the same fp32 steps as
+// load_chunk) so that the streaming loop keeps its registers.  One Philox
+// block per 4 consecutive tokens: counter (i / 4, position, row, 0), word
+// i % 4.  Tokens the count table lists (aux != 0) join with their exact values
+// elsewhere; NaN and -inf values take no part.
+template <bool BF16>
+__device__ __noinline__ void chunk_gmax(const unsigned char* ring, const uint32_t* msl, float rT, int ch, int nt,
+                                        bool full, const uint16_t* aux, int t0, uint32_t gpos, uint32_t row,
+                                        const uint64_t* seeds, unsigned long long* gmax) {
+  constexpr int VEC = BF16 ? 8 : 4;
+  const uint64_t seed = __ldg(seeds + row);
+  unsigned long long best = 0ull;
+  constexpr int NV = kPT / VEC;
+  for (int v = 0; v < NV; ++v) {
+    const int e0 = elem_index<VEC>(ch, v, 0);
+#pragma unroll
+    for (int hb = 0; hb < VEC / 4; ++hb) {
+      const int b0 = e0 + 4 * hb;
+      if (!full && b0 >= nt) break;
+      uint32_t c0 = (uint32_t)(t0 + b0) >> 2, c1 = gpos, c2 = row, c3 = 0u;
+      philox10(c0, c1, c2, c3, (uint32_t)seed, (uint32_t)(seed >> 32));
+      const uint32_t wd[4] = {c0, c1, c2, c3};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int li = b0 + k;
+        if (!full && li >= nt) break;
+        if (aux && aux[li] != 0u) continue;
+        const float xv = stream_value<BF16>(ring, msl, rT, li);
+        if (xv > -INFINITY) {
+          const float sc = __fadd_rn(xv, gumbel_of(word_to_uniform(wd[k])));
+          const unsigned long long pk = pack(f2key(sc), (uint32_t)(t0 + li));
+          best = pk > best ? pk : best;
+        }
+      }
+    }
+  }
+  if (best) atomicMax(gmax, best);
+}
+
 // Running (max, sum exp(x - max)) of one thread; -inf (and NaN) terms add nothing.
 __device__ __forceinline__ void lse_add(float& M, float& S, float v) {
   if (!(v > -INFINITY)) return;
@@ -505,7 +546,9 @@ __device__ __forceinline__ void lse_add(float& M, float& S, float v) {
 
 }  // namespace
 
-template <bool BF16>
+// EXACT: the variant that also keeps each exact-sampling segment's
+// Gumbel-max; without it none of that code is in the streaming loop.
+template <bool BF16, bool EXACT>
 __global__ void __launch_bounds__(kNT, 2) stage1_kernel(const Params P) {
   constexpr int ESZ = BF16 ? 2 : 4;
   constexpr int VEC = BF16 ? 8 : 4;
@@ -632,9 +675,12 @@ __global__ void __launch_bounds__(kNT, 2) stage1_kernel(const Params P) {
     const bool bias_on = (rc.flags & SS_BIAS) && P.bias != nullptr;
     const int jn = P.cu_draft ? min(j, gamma) : 0;
     const bool lse_on = P.cu_draft != nullptr && j < gamma && rc.stoch && !rc.trunc;
+    // exact sampling (a sample or bonus position of an SS_EXACT row): the
+    // segment's Gumbel-max of l_i + g_i over every token (Philox purpose 0)
+    const bool gmax_on = EXACT && rc.valid && rc.exact && (P.cu_draft == nullptr || j == gamma);
     const bool aux_on = rc.valid && (pen_on || bias_on);
     const int nflag = (pen_on ? rc.hist_len + jn : 0) + (bias_on ? rc.n_bias : 0);
-    const bool hashed = aux_on && !lse_on && nflag <= kHashMax;
+    const bool hashed = aux_on && !lse_on && !gmax_on && nflag <= kHashMax;
     const bool staged = aux_on && !hashed;
     const ss_bias_entry* brow = bias_on ? P.bias + (size_t)r * P.bias_stride : nullptr;
     const ss_bias_entry* bl = (bias_on && rc.n_bias <= kBiasPre) ? cb.bias : brow;
@@ -651,6 +697,7 @@ __global__ void __launch_bounds__(kNT, 2) stage1_kernel(const Params P) {
       sm.cnt[0] = sm.cnt[1] = sm.cnt[2] = 0;
       sm.nan_flag = 0;
       sm.nf = 0;
+      sm.gmax = 0ull;
       sm.rowbad = 0u;
     }
     if (hashed)
@@ -785,7 +832,7 @@ __global__ void __launch_bounds__(kNT, 2) stage1_kernel(const Params P) {
         // a one-chunk first stage takes the cut from the chunk it holds;
         // otherwise pass 0 scans the stage for the maxima first
         const bool merged = first && nch == 1;
-        const bool lazy = !first && full && !lse_on;
+        const bool lazy = !first && full && !lse_on && !gmax_on;
         for (int pass = (first && !merged) ? 0 : 1; pass < 2; ++pass) {
           uint32_t ck = pk_key(cutp);
           float cut_f = ck <= kKeyNegInf ? -INFINITY : key2f(ck);
@@ -934,6 +981,11 @@ __global__ void __launch_bounds__(kNT, 2) stage1_kernel(const Params P) {
           const bool isn = v != v;
           nan_seen |= isn;
           if (lse_on) lse_add(lM, lS, v);
+          if (gmax_on && v > -INFINITY) {
+            const float g = gumbel_of(philox_uniform(__ldg(P.seeds + r), (uint32_t)(t0 + li), rc.position + (uint32_t)j,
+                                                     (uint32_t)r, 0u));
+            atomicMax(&sm.gmax, pack(f2key(__fadd_rn(v, g)), (uint32_t)(t0 + li)));
+          }
           const unsigned long long pk = pack(isn ? kKeyNegInf : f2key(v), (uint32_t)(t0 + li));
           if (pk >= cutp) append(pk);
         };
@@ -991,6 +1043,14 @@ __global__ void __launch_bounds__(kNT, 2) stage1_kernel(const Params P) {
         cutp = (nt >= kK && added == need_s && mn > base_cut) ? mn : base_cut;
         n_end = n + added;
       }
+      // exact sampling: the stage's Gumbel-max, read from the slot before it is
+      // refilled (and from the stage's count table, still in place)
+      if (gmax_on) {
+        for (int ch = 0; ch < nch; ++ch)
+          chunk_gmax<BF16>(ring, msl, rc.rT, ch, nt, full, staged ? aux : nullptr, t0, rc.position + (uint32_t)j,
+                           (uint32_t)r, P.seeds, &sm.gmax);
+        __syncthreads();  // every read of the slot is done before its refill
+      }
       // refill this slot with the stage NS ahead (every read of it is done)
       if (tid == 0 && g + NS < g1) {
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -1040,6 +1100,7 @@ __global__ void __launch_bounds__(kNT, 2) stage1_kernel(const Params P) {
         const double S = block_sum_d(part, sm.red);
         if (tid == 0) P.ws.tile_lse[lslot] = make_float2(Mb, (float)S);
       }
+      if (gmax_on && tid == 0) P.ws.tile_gmax[lslot] = sm.gmax;  // updates end before select_top's barriers
     } else {  // invalid row parameters: stage 2 reports the row
       for (int q = tid; q < kK; q += kNT) stg[q] = 0ull;
       if (tid == 0) P.ws.tile_status[lslot] = 0u;
@@ -1070,16 +1131,24 @@ __global__ void __launch_bounds__(kNT, 2) stage1_kernel(const Params P) {
   }
 }
 
-template __global__ void stage1_kernel<false>(const Params);
-template __global__ void stage1_kernel<true>(const Params);
+template __global__ void stage1_kernel<false, false>(const Params);
+template __global__ void stage1_kernel<true, false>(const Params);
+template __global__ void stage1_kernel<false, true>(const Params);
+template __global__ void stage1_kernel<true, true>(const Params);
 
-const void* stage1_ptr(bool bf16) {
-  return bf16 ? (const void*)stage1_kernel<true> : (const void*)stage1_kernel<false>;
+const void* stage1_ptr(bool bf16, bool exact) {
+  if (exact) return bf16 ? (const void*)stage1_kernel<true, true> : (const void*)stage1_kernel<false, true>;
+  return bf16 ? (const void*)stage1_kernel<true, false> : (const void*)stage1_kernel<false, false>;
 }
 
-void stage1_launch(bool bf16, int grid, size_t smem, cudaStream_t st, const Params& P) {
-  if (bf16) stage1_kernel<true><<<grid, kNT, smem, st>>>(P);
-  else stage1_kernel<false><<<grid, kNT, smem, st>>>(P);
+void stage1_launch(bool bf16, bool exact, int grid, size_t smem, cudaStream_t st, const Params& P) {
+  if (exact) {
+    if (bf16) stage1_kernel<true, true><<<grid, kNT, smem, st>>>(P);
+    else stage1_kernel<false, true><<<grid, kNT, smem, st>>>(P);
+  } else {
+    if (bf16) stage1_kernel<true, false><<<grid, kNT, smem, st>>>(P);
+    else stage1_kernel<false, false><<<grid, kNT, smem, st>>>(P);
+  }
 }
 
 size_t stage1_smem_bytes(int BN, bool bf16, int nslot) { return layout(BN, bf16 ? 2 : 4, nslot).total; }

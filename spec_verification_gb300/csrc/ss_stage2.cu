@@ -328,6 +328,8 @@ __global__ void __launch_bounds__(kNT2, 9) stage2_kernel(const Params P, int ver
         uint32_t st = 0u;
         if (no_finite) st |= SS_ST_NO_FINITE;
         else if (pos_inf) st |= SS_ST_POS_INF;
+        // SS_EXACT on a plan without exact sampling: sampled from the candidates
+        if (rc.exact && !P.exact_on && !is_draft && !point) st |= SS_ST_NOT_EXACT;
 
         // ---- 3. token of this position (sample / bonus)
         int32_t token = -1;
@@ -338,6 +340,16 @@ __global__ void __launch_bounds__(kNT2, 9) stage2_kernel(const Params P, int ver
             token = -1;
           } else if (point) {
             token = tok0;
+          } else if (rc.exact && P.exact_on) {
+            // exact sampling: the Gumbel-max over the whole vocabulary, the
+            // largest of the segments' maxima (stage 1)
+            unsigned long long gb = 0ull;
+            for (int t = lane; t < nseg; t += 32) {
+              const unsigned long long v = P.ws.tile_gmax[tbase + t];
+              gb = v > gb ? v : gb;
+            }
+            gb = warp_max_u64(gb);
+            token = gb ? pk_tok(gb) : tok0;
           } else {
             unsigned long long sc = 0ull;
 #pragma unroll

@@ -48,7 +48,7 @@ class Out(C.Structure):
 
 EXPORTS = ["ss_plan_create", "ss_plan_destroy", "ss_workspace_bytes", "ss_plan_tile",
            "ss_plan_num_tiles", "ss_plan_stage1_ctas", "ss_sample", "ss_verify", "ss_status_str", "ss_last_error",
-           "ss_workspace_diag_offset", "ss_sample_noalloc"]
+           "ss_workspace_diag_offset", "ss_sample_noalloc", "ss_plan_enable_exact"]
 
 _lib = None
 
@@ -76,6 +76,9 @@ def library() -> C.CDLL:
     L.ss_plan_num_tiles.restype = C.c_int32
     L.ss_plan_stage1_ctas.argtypes = [C.c_void_p]
     L.ss_plan_stage1_ctas.restype = C.c_int32
+    if hasattr(L, "ss_plan_enable_exact"):
+        L.ss_plan_enable_exact.argtypes = [C.c_void_p, C.c_int]
+        L.ss_plan_enable_exact.restype = C.c_int
     L.ss_sample.argtypes = [C.c_void_p, C.POINTER(Batch), C.c_void_p, C.c_void_p, C.c_void_p,
                             C.c_void_p, C.POINTER(Out)]
     L.ss_sample.restype = C.c_int
@@ -114,6 +117,10 @@ class Plan:
         self.stage1_ctas = L.ss_plan_stage1_ctas(self._p)
         self.workspace_bytes = L.ss_workspace_bytes(self._p)
         self.diag_offset = L.ss_workspace_diag_offset(self._p)
+
+    def enable_exact(self, on: bool = True):
+        """Run the exact-sampling variant of stage 1 (rows flagged SS_EXACT)."""
+        _check(library().ss_plan_enable_exact(self._p, 1 if on else 0))
 
     @property
     def handle(self):

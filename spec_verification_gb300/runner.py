@@ -71,6 +71,8 @@ class DeviceRun:
         npos = w.n_positions
         self.plan = native.Plan(w.V, w.B, max_positions or npos, w.dtype,
                                 w.q_dtype if self.verify else "f32", tile, self.dev.index or 0)
+        if (w.meta or {}).get("exact_sampling"):
+            self.plan.enable_exact(True)
         host = {
             "logits": _as_torch_bits(_padded_rows(w.logits, 2 if w.dtype == "bf16" else 4)),
             "rows": _as_torch_bits(pack_rows(w.rows, w.B)),

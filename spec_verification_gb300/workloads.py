@@ -41,6 +41,7 @@ TOPK = 1 << 4
 TOPP = 1 << 5
 MINP = 1 << 6
 BOUNDED_P = 1 << 7   # verify against the candidate softmax even without truncation
+EXACT = 1 << 8       # untruncated rows sample over the whole vocabulary
 
 ROW_FIELDS = ("flags", "temperature", "top_p", "min_p", "rep", "freq", "pres",
               "top_k", "hist_len", "n_bias", "position")
@@ -470,6 +471,17 @@ def with_bounded_p(w: Workload) -> Workload:
     stoch = (w.rows["flags"] & GREEDY) == 0
     w.rows["flags"][stoch] |= np.uint32(BOUNDED_P)
     w.name = w.name + "_bounded"
+    return w
+
+
+def with_exact_sampling(w: Workload) -> Workload:
+    """The same batch with every stochastic row untruncated and flagged EXACT
+    (sampled over the whole vocabulary; the plan runs exact sampling)."""
+    stoch = (w.rows["flags"] & GREEDY) == 0
+    w.rows["flags"][stoch] &= ~np.uint32(TOPK | TOPP | MINP)
+    w.rows["flags"][stoch] |= np.uint32(EXACT)
+    w.meta = dict(w.meta, exact_sampling=True)
+    w.name = w.name + "_exact"
     return w
 
 

@@ -60,7 +60,7 @@ def test_flag_values_agree():
     text = HEADER.read_text()
     for name, val in [("SS_GREEDY", W.GREEDY), ("SS_MASK", W.MASK), ("SS_PENALTY", W.PENALTY),
                       ("SS_BIAS", W.BIAS), ("SS_TOPK", W.TOPK), ("SS_TOPP", W.TOPP), ("SS_MINP", W.MINP),
-                      ("SS_BOUNDED_P", W.BOUNDED_P)]:
+                      ("SS_BOUNDED_P", W.BOUNDED_P), ("SS_EXACT", W.EXACT)]:
         m = re.search(name + r" = 1u << (\d+)", text)
         assert m and (1 << int(m.group(1))) == val, name
 

@@ -262,6 +262,45 @@ def test_verify_bounded_p_rows():
     assert np.any(ora["num_accepted"][stoch] < 3)
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_exact_sampling(dtype):
+    # SS_EXACT on untruncated stochastic rows (sample positions): the
+    # Gumbel-max over the whole vocabulary, with processors on (listed tokens
+    # through the count tables), ragged last tile, greedy and truncated rows
+    # beside them
+    w = W.sample_workload(seed=36, B=40, V=50003, dtype=dtype, name="exact")
+    stoch = (w.rows["flags"] & F.GREEDY) == 0
+    untr = stoch & (np.arange(w.B) % 3 != 0)
+    w.rows["flags"][untr] &= ~np.uint32(F.TOPK | F.TOPP | F.MINP)
+    w.rows["flags"][stoch] |= np.uint32(F.EXACT)
+    w.meta["exact_sampling"] = True
+    gpu, ora, _ = check(w)
+    # some exact samples fall outside the 128 candidates
+    outside = [r for r in np.where(untr)[0] if gpu["tokens"][r] not in set(gpu["cand_ids"][r])]
+    assert len(outside) >= 1
+
+
+def test_exact_sampling_verify_bonus():
+    # the bonus token of a verify row flagged SS_EXACT
+    w = W.verify_workload(37, 16, 30000, [0, 1, 0, 2, 0, 0, 1, 0, 3, 0, 0, 1, 0, 0, 2, 0], "bf16", "bf16",
+                          processors=True, noise=0.2)
+    stoch = (w.rows["flags"] & F.GREEDY) == 0
+    w.rows["flags"][stoch] &= ~np.uint32(F.TOPK | F.TOPP | F.MINP)
+    w.rows["flags"][stoch] |= np.uint32(F.EXACT)
+    w.meta["exact_sampling"] = True
+    check(w)
+
+
+def test_exact_flag_without_exact_plan():
+    # SS_EXACT on a plan without exact sampling: candidates' sample, status bit
+    w = W.sample_workload(seed=38, B=24, V=30000, dtype="bf16", name="notexact")
+    stoch = (w.rows["flags"] & F.GREEDY) == 0
+    w.rows["flags"][stoch] &= ~np.uint32(F.TOPK | F.TOPP | F.MINP)
+    w.rows["flags"][stoch] |= np.uint32(F.EXACT)
+    gpu, ora, _ = check(w)
+    assert np.all((gpu["row_status"][stoch] & (1 << 8)) != 0)
+
+
 def test_verify_edge_cases():
     rng = np.random.default_rng(34)
     V = 9000

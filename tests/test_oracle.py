@@ -515,6 +515,45 @@ def test_bounded_p_is_the_full_p_when_v_is_at_most_128():
     np.testing.assert_array_equal(a["num_accepted"], b["num_accepted"])
 
 
+def test_exact_sampling_reaches_beyond_the_candidates():
+    """SS_EXACT: an untruncated row samples by the Gumbel-max over the whole
+    vocabulary, so the token follows the full softmax (Gumbel-max theorem):
+    with 400 equal logits every token has probability 1/400, while the
+    bounded sampler only ever returns one of the 128 candidates (0..127)."""
+    V, B = 400, 40000
+    x = np.zeros((B, V), np.float32)
+    seeds = np.arange(B, dtype=np.uint64) * 6151 + 7
+    a = O.sample(sample_case(x, flags=0, seeds=seeds))
+    wb = sample_case(x, flags=F.EXACT, seeds=seeds)
+    wb.meta["exact_sampling"] = True
+    b = O.sample(wb)
+    assert a["tokens"].max() < 128
+    counts = np.bincount(b["tokens"], minlength=V)
+    assert chi2_pvalue(counts, np.full(V, 1.0 / V)) > 1e-4
+    assert np.all(b["row_status"] == 0)
+    # truncating rows ignore the flag
+    wc = sample_case(x[:2000], flags=F.EXACT | F.TOPK, top_k=50, seeds=seeds[:2000])
+    wc.meta["exact_sampling"] = True
+    c = O.sample(wc)
+    assert c["tokens"].max() < 50
+    # without exact sampling enabled: the candidates' sample and a status bit
+    d = O.sample(sample_case(x[:2000], flags=F.EXACT, seeds=seeds[:2000]))
+    np.testing.assert_array_equal(d["tokens"], a["tokens"][:2000])
+    assert np.all(d["row_status"] == 1 << 8)
+
+
+def test_exact_sampling_equals_bounded_when_v_is_at_most_128():
+    rng = np.random.default_rng(44)
+    V, B = 100, 2000
+    x = (rng.standard_normal((B, V)) * 2).astype(np.float32)
+    seeds = np.arange(B, dtype=np.uint64) + 3
+    a = O.sample(sample_case(x, flags=0, seeds=seeds))
+    wb = sample_case(x, flags=F.EXACT, seeds=seeds)
+    wb.meta["exact_sampling"] = True
+    b = O.sample(wb)
+    np.testing.assert_array_equal(a["tokens"], b["tokens"])
+
+
 def test_golden_rejection_closed_forms():
     fx = json.load(open(os.path.join(GOLDEN, "rejection_examples.json")))[0]
     p = np.array(fx["p"])
