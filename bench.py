@@ -190,9 +190,17 @@ def whole_job_rate(world: int, rows: int, steps: int, ms: float) -> float:
 
 
 def num_segments(npos: int, z: int, ctas: int) -> int:
-    """Segments of the stage-1 split: the npos * z tiles are cut into
-    g = min(ctas, npos * z) contiguous runs (run c starts at c * T // g), and
+    """Segments of the stage-1 split: with two or more CTAs per position each
+    position is cut into kk = ceil(z / ceil(z / k)) ranges (k = ctas // npos),
+    one segment each; otherwise the npos * z tiles are cut into
+    g = min(ctas, npos * z) contiguous runs (run c starts at c * T // g) and
     each (run, position) overlap is one segment."""
+    if npos <= 0:
+        return 0
+    k = ctas // npos
+    if k >= 2:
+        lr = -(-z // k)
+        return npos * (-(-z // lr))
     T = npos * z
     g = min(ctas, T)
     starts = [c * T // g for c in range(g)]

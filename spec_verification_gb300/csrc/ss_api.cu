@@ -281,11 +281,18 @@ int mask_rows_copyable(const ss::Params& P) {
 // least L stages.  A call has at least B positions (exactly B when sampling),
 // and once B * Z_v >= grid1 the ranges are at least floor(B * Z_v / grid1)
 // stages long; below that a range may be a single stage.
+// Under the aligned split (two or more stage-1 CTAs per position) a position
+// has kk <= grid1 / npos <= grid1 / B lists.
 int seg_cap_for(const ss_plan* pl, int B) {
-  const long long tmin = (long long)std::min(B, pl->max_positions) * pl->Z;
-  if (tmin < pl->grid1) return pl->Z;
-  const long long L = tmin / pl->grid1;
-  return (int)std::min<long long>(pl->Z, 1 + (pl->Z - 1 + L - 1) / L);
+  const int bmin = std::max(1, std::min(B, pl->max_positions));
+  const long long tmin = (long long)bmin * pl->Z;
+  int cap = pl->Z;
+  if (tmin >= pl->grid1) {
+    const long long L = tmin / pl->grid1;
+    cap = (int)std::min<long long>(pl->Z, 1 + (pl->Z - 1 + L - 1) / L);
+  }
+  if (pl->grid1 / bmin >= 2) cap = std::max(cap, std::min(pl->Z, pl->grid1 / bmin));
+  return cap;
 }
 
 ss_status launch(const ss_plan* pl, const ss::Params& P0, cudaStream_t st, bool verify, void* const* ev) {

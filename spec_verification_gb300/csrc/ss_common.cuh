@@ -252,14 +252,42 @@ __device__ __forceinline__ int num_positions(const Params& P) {
   return min(n, P.max_positions);
 }
 
-// Segment split shared by stage 1 and stage 2.  The T = npos * Z stages
-// (position-major) are cut into G = min(grid1, T) contiguous ranges; CTA c of
-// stage 1 owns stages [seg_start(c), seg_start(c + 1)), at least one each.
-__device__ __forceinline__ long long seg_start(long long c, long long T, long long G) { return c * T / G; }
+// Segment split shared by stage 1 and stage 2: the T = npos * Z stages
+// (position-major) are cut into G contiguous ranges, CTA c of stage 1 owning
+// stages [seg_start(c), seg_start(c + 1)), at least one each.
+//  - aligned (when the stage-1 grid holds two or more CTAs per position):
+//    each position is cut into kk ranges of Lr stages (the last may be
+//    shorter), so that no range crosses a position boundary and every CTA has
+//    exactly one segment;
+//  - even (otherwise): G = min(grid1, T) ranges of T / G stages.
+struct Split {
+  long long T;
+  int G, kk, Lr;
+  bool aligned;
+};
+__device__ __forceinline__ Split make_split(const Params& P, int npos) {
+  Split s;
+  s.T = (long long)npos * P.Z;
+  const int k = npos > 0 ? P.grid1 / npos : 0;
+  s.aligned = k >= 2;
+  if (s.aligned) {
+    s.Lr = (P.Z + k - 1) / k;
+    s.kk = (P.Z + s.Lr - 1) / s.Lr;
+    s.G = npos * s.kk;
+  } else {
+    s.kk = s.Lr = 0;
+    s.G = (int)(s.T < (long long)P.grid1 ? s.T : (long long)P.grid1);
+  }
+  return s;
+}
+__device__ __forceinline__ long long seg_start(const Split& s, long long c, int Z) {
+  if (s.aligned) return (c / s.kk) * Z + (c % s.kk) * s.Lr;
+  return c * s.T / s.G;
+}
 // The CTA whose range holds stage g: the largest c with seg_start(c) <= g.
-__device__ __forceinline__ int seg_cta(long long g, long long T, long long G) { return (int)(((g + 1) * G - 1) / T); }
-__device__ __forceinline__ long long seg_grid(const Params& P, long long T) {
-  return T < (long long)P.grid1 ? T : (long long)P.grid1;
+__device__ __forceinline__ int seg_cta(const Split& s, long long g, int Z) {
+  if (s.aligned) return (int)((g / Z) * s.kk + (g % Z) / s.Lr);
+  return (int)(((g + 1) * s.G - 1) / s.T);
 }
 
 // ------------------------------------------------------------------ block helpers

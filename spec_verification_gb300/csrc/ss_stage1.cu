@@ -573,11 +573,10 @@ __global__ void __launch_bounds__(kNT, 2) stage1_kernel(const Params P) {
   const int V = P.V, Z = P.Z;
   if (blockIdx.x == 0 && tid == 0) *P.ws.resid_count = 0u;  // residual queue of this call
   const int npos = num_positions(P);
-  const long long T = (long long)npos * Z;
-  if (T <= 0) return;
-  const long long G = seg_grid(P, T);
-  if ((long long)blockIdx.x >= G) return;
-  const long long g0 = seg_start(blockIdx.x, T, G), g1 = seg_start(blockIdx.x + 1, T, G);
+  const Split sp = make_split(P, npos);
+  if (sp.T <= 0) return;
+  if ((int)blockIdx.x >= sp.G) return;
+  const long long g0 = seg_start(sp, blockIdx.x, Z), g1 = seg_start(sp, blockIdx.x + 1, Z);
   const bool mask_tma = P.mask_tma != 0 && P.bitmask != nullptr;
   const int nch = BN / kChunk;
 
@@ -621,10 +620,13 @@ __global__ void __launch_bounds__(kNT, 2) stage1_kernel(const Params P) {
       }
     asm volatile("cp.async.commit_group;" ::: "memory");
   };
-  // staging list of position pos for this CTA's segment
+  // staging list of position pos for this CTA's segment: list index
+  // blockIdx.x - (the CTA holding the position's first stage), which is 0 for
+  // every position of the range but the first (they start inside it)
+  const int pos_first = (int)(g0 / Z);
+  const int first_off = (int)blockIdx.x - seg_cta(sp, (long long)pos_first * Z, Z);
   auto slot_of = [&](int pos) -> size_t {
-    const long long gs = (long long)pos * Z;
-    return (size_t)gs + (size_t)((long long)blockIdx.x - seg_cta(gs, T, G));
+    return (size_t)pos * Z + (size_t)(pos == pos_first ? first_off : 0);
   };
 
   if (tid == 0) {

@@ -102,7 +102,7 @@ __global__ void __launch_bounds__(kNT2, 9) stage2_kernel(const Params P, int ver
   const int npos = num_positions(P);
   const int V = P.V, Z = P.Z;
   const int need = min(kK, V);
-  const long long T = (long long)npos * Z, G = seg_grid(P, T);
+  const Split sp = make_split(P, npos);
 
   for (int pos = blockIdx.x; pos < npos; pos += gridDim.x) {
     // ---- the position's reads: row lookup (warp 0) beside the lists (all);
@@ -116,7 +116,7 @@ __global__ void __launch_bounds__(kNT2, 9) stage2_kernel(const Params P, int ver
       sm.accept = 0;
       sm.lse = 0.0;
     }
-    const int nseg = seg_cta((long long)pos * Z + Z - 1, T, G) - seg_cta((long long)pos * Z, T, G) + 1;
+    const int nseg = seg_cta(sp, (long long)pos * Z + Z - 1, Z) - seg_cta(sp, (long long)pos * Z, Z) + 1;
     const size_t tbase = (size_t)pos * Z;
     if (warp == 0) {
       int r = pos, c0 = 0, c1 = 0;
