@@ -388,6 +388,7 @@ def run_ours(args, w, desc):
                "steps": E, "ms_per_step": ems / E}
         del hrun
 
+    diag = run.diag()
     peak, peak_kind = read_peaks()
     tile = run.plan.tile
     alg1 = stage1_alg_bytes(w, tile, run.plan.stage1_ctas)
@@ -419,6 +420,10 @@ def run_ours(args, w, desc):
             "clocks": ck,
             "e2e": e2e,
             "gpu_launches": K * (3 if verify else 2),
+            # stage-1 self-checks over every call of the run: stages resolved by
+            # the exact fallback, and bulk copies that did not land in time
+            # (nonzero: the run's results are not valid)
+            "self_check": {"stage_fallbacks": int(diag[0]), "copy_timeouts": int(diag[3])},
             "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)
