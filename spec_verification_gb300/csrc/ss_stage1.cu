@@ -339,10 +339,13 @@ __device__ __noinline__ unsigned long long compact(unsigned long long* cand, uns
 // Raise the cut with one 256-bin histogram of the buffer over [cut, max]: the
 // new cut is the lower edge of the bin holding the 128th largest entry, so at
 // least 128 entries stay at or above it, and the entries below it leave the
-// buffer.  Returns the new cut (never below `cut`) and the new count in
-// sm.out_cnt.  Entries below `cut` (left by a stage fallback) count in bin 0.
-__device__ __noinline__ unsigned long long raise_cut(unsigned long long* cand, unsigned long long* tmp, int n,
-                                                     unsigned long long cut, S1Smem& sm) {
+// buffer.  Returns the new cut (never below `cut`) and the new count.  Entries below `cut` (left by a stage fallback) count in bin 0.
+struct Raised {
+  unsigned long long cut;
+  int n;
+};
+__device__ __noinline__ Raised raise_cut(unsigned long long* cand, unsigned long long* tmp, int n,
+                                         unsigned long long cut, S1Smem& sm) {
   const int tid = threadIdx.x;
   if (tid < 256) sm.sel.hist[tid] = 0u;
   if (tid == 0) sm.out_cnt = 0;
@@ -356,9 +359,8 @@ __device__ __noinline__ unsigned long long raise_cut(unsigned long long* cand, u
   boundary_bin(sm.sel, kK);
   const int bstar = mx > cut ? sm.sel.bstar : 0;
   if (bstar <= 0) {  // no progress: keep everything
-    if (tid == 0) sm.out_cnt = n;
     __syncthreads();
-    return cut;
+    return Raised{cut, n};
   }
   const unsigned long long nc = cut + ((unsigned long long)bstar << shift);
   for (int i = tid; i < n; i += kNT) {
@@ -366,10 +368,14 @@ __device__ __noinline__ unsigned long long raise_cut(unsigned long long* cand, u
     if (c >= nc) tmp[atomicAdd(&sm.out_cnt, 1)] = c;
   }
   __syncthreads();
+  // the count is returned, read before the final barrier: a caller that read
+  // sm.out_cnt after it could race with thread 0 resetting it for the next
+  // selection (compact, the segment end), and a warp that saw the reset count
+  // would take other branches (and barriers) than the rest of the block
   const int m = sm.out_cnt;
   for (int i = tid; i < m; i += kNT) cand[i] = tmp[i];
   __syncthreads();
-  return nc;
+  return Raised{nc, m};
 }
 
 // Load chunk ch of the stage and apply mask and temperature; returns the
@@ -1061,8 +1067,9 @@ __global__ void __launch_bounds__(kNT, 2) stage1_kernel(const Params P) {
       // ---- keep room in the buffer: one histogram pass raises the cut; the
       // exact top-128 only if that left too many (a crowd of equal values)
       if (rc.valid && n_end > kRaiseAt) {
-        cutp = raise_cut(cand, tmp, n_end, cutp, sm);
-        n_end = sm.out_cnt;
+        const Raised rz = raise_cut(cand, tmp, n_end, cutp, sm);
+        cutp = rz.cut;
+        n_end = rz.n;
         if (n_end > kCompactAt) {
           cutp = compact(cand, tmp, outb, n_end, sm);
           n_end = kK;
