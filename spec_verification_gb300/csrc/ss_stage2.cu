@@ -41,6 +41,8 @@ struct S2Smem {
   unsigned long long srt[kK];  // the same, ordered
   double w[kK];                // exp(l_t - l_0) of the ordered candidates (stochastic rows)
   float g[kK];                 // their Gumbel noise: sample (purpose 0) or residual (purpose 2)
+  float qv[kK];                // their draft probability q (truncated draft positions)
+  float u_acc;                 // the acceptance uniform (draft positions)
   unsigned long long slots[kNT / 32];
   double lse;
   int r, j, gamma, c0, cnt, out_cnt, last, token, accept, d;
@@ -235,7 +237,14 @@ __global__ void __launch_bounds__(kNT2, 9) stage2_kernel(const Params P, int ver
         // of a sampled / bonus position, or the truncated residual's of a draft
         if (rc.stoch && (!is_draft || rc.trunc) && tid < need && c != 0ull)
           sm.g[tid] = gumbel_of(philox_uniform(seed, (uint32_t)pk_tok(c), position, (uint32_t)r, is_draft ? 2u : 0u));
+        // a truncated draft position's residual needs q at every kept
+        // candidate: fetched here, one per thread, off the epilogue's chain
+        if (is_draft && rc.stoch && rc.trunc && tid < need && c != 0ull) {
+          const int32_t tk = pk_tok(c);
+          sm.qv[tid] = P.q ? load_scalar(P.q, P.q_bf16, ((int64_t)c0 + j) * P.ld_q + tk) : (tk == sm.d ? 1.0f : 0.0f);
+        }
       }
+      if (tid == 0 && is_draft && rc.stoch) sm.u_acc = philox_uniform(seed, 0u, position, (uint32_t)r, 1u);
       __syncthreads();
 
       if (warp == 0) {
@@ -374,13 +383,12 @@ __global__ void __launch_bounds__(kNT2, 9) stage2_kernel(const Params P, int ver
             accept = (d_ok && d == tok0) ? 1 : 0;
             token = tok0;
           } else {
-            const int64_t qrow = (int64_t)c0 + j;
             double pd = 0.0;
             if (rc.trunc) {
               double mine = 0.0;
 #pragma unroll
               for (int k = 0; k < 4; ++k)
-                if (4 * lane + k < nk && tok[k] == d) mine = w[k] / zk;
+                if (4 * lane + k < nk && tok[k] == d) mine = w[k] * izk;
 #pragma unroll
               for (int dd = 16; dd > 0; dd >>= 1) mine = fmax(mine, __shfl_xor_sync(0xffffffffu, mine, dd));
               pd = mine;
@@ -412,7 +420,7 @@ __global__ void __launch_bounds__(kNT2, 9) stage2_kernel(const Params P, int ver
               if (d_ok) pd = exp((double)dl - lse);
             }
             if (d_ok) {
-              const float u = philox_uniform(seed, 0u, position, (uint32_t)r, 1u);
+              const float u = sm.u_acc;
               const float prod = __fmul_rn(u, sm.qd);
               accept = (pd > 0.0 && (double)prod <= pd) ? 1 : 0;
             }
@@ -425,8 +433,7 @@ __global__ void __launch_bounds__(kNT2, 9) stage2_kernel(const Params P, int ver
                 for (int k = 0; k < 4; ++k) {
                   rr[k] = 0.0;
                   if (4 * lane + k < nk)
-                    rr[k] = fmax(0.0, w[k] * izk - (P.q ? (double)load_scalar(P.q, P.q_bf16, qrow * P.ld_q + tok[k])
-                                                        : (tok[k] == d ? 1.0 : 0.0)));
+                    rr[k] = fmax(0.0, w[k] * izk - (double)sm.qv[4 * lane + k]);
                   pos_any |= (4 * lane + k < nk && rr[k] > 0.0);
                 }
                 const bool anypos = __any_sync(0xffffffffu, pos_any);
