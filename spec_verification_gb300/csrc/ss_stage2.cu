@@ -50,6 +50,20 @@ struct S2Smem {
   uint32_t status;
 };
 
+// Merges (m2, s2) into the running (max, sum exp(x - max)) pair (m, s);
+// pairs with m = -inf add nothing.
+__device__ __forceinline__ void lse_merge(float& m, float& s, float m2, float s2) {
+  if (!(m2 > -INFINITY)) return;
+  if (!(m > -INFINITY)) {
+    m = m2;
+    s = s2;
+    return;
+  }
+  const float mx = fmaxf(m, m2);
+  s = s * expf(m - mx) + s2 * expf(m2 - mx);
+  m = mx;
+}
+
 // Processed logit of one token at one position (the same fp32 steps as the
 // stage-1 prelude), for a draft token outside the candidate list.  One warp.
 __device__ float prelude_single_warp(const Params& P, const RowCtx& rc, int pos, int r, int c0, int jn, int tok,
@@ -393,15 +407,21 @@ __global__ void __launch_bounds__(kNT2, 9) stage2_kernel(const Params P, int ver
               for (int dd = 16; dd > 0; dd >>= 1) mine = fmax(mine, __shfl_xor_sync(0xffffffffu, mine, dd));
               pd = mine;
             } else {
-              // full-vocabulary softmax: LSE from the segments' (max, sum exp) partials
-              float M = -INFINITY;
-              for (int tt = 0; tt < nseg; ++tt) M = fmaxf(M, P.ws.tile_lse[tbase + tt].x);
-              double S = 0.0;
-              for (int tt = 0; tt < nseg; ++tt) {
+              // full-vocabulary softmax: LSE from the segments' (max, sum exp)
+              // partials, lane-parallel in fp32 (the partials are fp32 sums;
+              // this acceptance test is held to 1e-5 relative)
+              float M = -INFINITY, S = 0.0f;
+              for (int tt = lane; tt < nseg; tt += 32) {
                 const float2 ms = P.ws.tile_lse[tbase + tt];
-                if (ms.x > -INFINITY) S += (double)ms.y * exp((double)ms.x - (double)M);
+                lse_merge(M, S, ms.x, ms.y);
               }
-              lse = (double)M + log(S);
+#pragma unroll
+              for (int dd = 16; dd > 0; dd >>= 1) {
+                const float M2 = __shfl_xor_sync(0xffffffffu, M, dd);
+                const float S2 = __shfl_xor_sync(0xffffffffu, S, dd);
+                lse_merge(M, S, M2, S2);
+              }
+              lse = (double)(M + logf(S));
               // d among the candidates: its logit; else recompute it
               bool found = false;
               float dl = 0.0f;
@@ -417,7 +437,7 @@ __global__ void __launch_bounds__(kNT2, 9) stage2_kernel(const Params P, int ver
               } else if (d_ok) {
                 dl = prelude_single_warp(P, rc, pos, r, c0, min(j, gamma), d, lane);
               }
-              if (d_ok) pd = exp((double)dl - lse);
+              if (d_ok) pd = (double)expf(dl - (float)lse);
             }
             if (d_ok) {
               const float u = sm.u_acc;
