@@ -180,7 +180,10 @@ def verify(w, exact: bool = False, rows=None, tokens_stride: int | None = None) 
 
 
 def prelude(w, r: int, pos: int, extra=()) -> tuple[np.ndarray, int]:
-    """Processed logits of one position (row r, target position pos)."""
+    """Processed logits of row r at target position pos, where pos is the
+    absolute position (the logits row, not the index within row r) and extra
+    holds the tokens appended to the row's history (a verify position's
+    earlier drafts)."""
     keep: list = []
     P = _problem(w, keep)
     ex = np.ascontiguousarray(np.asarray(extra, np.int32))

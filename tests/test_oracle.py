@@ -612,6 +612,34 @@ def test_mass_outside_top128_report():
     assert m[2] > 0.9 and m[3] > 0.9          # near-flat rows: nearly all mass outside
 
 
+def test_packed16_staging_report():
+    """The 16-bit-key report's full-precision side is the oracle's candidate
+    set; its packed side loses exactly the two things a 16-bit key beside a
+    tile-local index drops: mantissa bits below bf16 and the global token
+    order among equal keys in different tiles."""
+    from tests import key16_report as R
+    w = W.topk_stress_workload(3, 4, 40000)
+    out = O.sample(w)
+    for r in range(w.B):
+        assert R.full_key_set(R.position_logits(w, r)) == set(out["cand_ids"][r].tolist())
+    # distinct bf16 values: the 16-bit keys are the full keys, so both sets agree
+    bits = np.random.default_rng(0).permutation(np.arange(0x3F80, 0x3F80 + 2 * R.TILE)).astype(np.uint16)
+    x = W.bf16_bits_to_f32(bits)
+    assert R.packed16_set(x) == R.full_key_set(x)
+    # precision: 1 + 2^-10 rounds into 1's 16-bit key, so the lower token wins
+    x = np.full(R.TILE, -10.0, np.float32)
+    x[:R.K - 1] = 5.0
+    x[200], x[300] = 1.0, 1.0 + 2.0 ** -10
+    assert 300 in R.full_key_set(x) and 200 in R.packed16_set(x)
+    assert R.full_key_set(x) - R.packed16_set(x) == {300}
+    # equal values in two tiles: the tile-local index decides, not the token
+    x = np.full(2 * R.TILE, -10.0, np.float32)
+    x[100:100 + R.K - 1] = 5.0
+    x[5], x[R.TILE + 3] = 1.0, 1.0
+    assert R.full_key_set(x) - R.packed16_set(x) == {5}
+    assert R.packed16_set(x) - R.full_key_set(x) == {R.TILE + 3}
+
+
 def test_config1_reference_behaviour():
     c = W.config1()
     out = O.sample(c)
