@@ -107,8 +107,11 @@ enum {
   SS_ST_BAD_DRAFT = 1u << 5,   /* a draft id outside [0, V): rejected */
   SS_ST_POS_INF = 1u << 6,     /* +inf processed logit: point mass on it */
   SS_ST_RESID_EMPTY = 1u << 7, /* residual max(0, p - q) had no mass: sampled from p */
-  SS_ST_NOT_EXACT = 1u << 8     /* SS_EXACT on a plan without exact sampling:
+  SS_ST_NOT_EXACT = 1u << 8,    /* SS_EXACT on a plan without exact sampling:
                                    sampled from the 128 candidates */
+  SS_ST_CAPACITY = 1u << 9      /* verification: the row's target positions reach
+                                   past the plan's max_positions; not verified,
+                                   tokens -1, num_accepted 0 */
 };
 
 /* One row's sampling parameters (device array of B entries, 44 bytes each).
@@ -173,7 +176,11 @@ typedef struct {
 } ss_out;
 
 /* Create a plan.  V in [1, 2^20]; max_rows >= 1; max_positions >= max_rows
- * bounds B_pos (B for sampling, cu_draft[B] + B for verification);
+ * bounds B_pos (B for sampling, cu_draft[B] + B for verification; a
+ * verification call whose device-side cu_draft[B] + B exceeds it verifies
+ * the rows whose positions all lie below max_positions and reports the
+ * others with SS_ST_CAPACITY; candidate outputs are written for positions
+ * below max_positions only);
  * tile = 0 chooses B_N automatically, else 8192 or 16384.  device is the
  * CUDA ordinal the plan is for.  Returns SS_ERR_ARG / SS_ERR_UNSUPPORTED on
  * bad sizes; *plan is NULL on failure.  The plan is host memory owned by the
@@ -280,8 +287,11 @@ const char* ss_status_str(ss_status s);
 const char* ss_last_error(void);
 
 /* Byte offset, inside the workspace, of 8 uint32 diagnostic counters the
- * kernels increment (0: stage-1 tiles that took the generic radix path,
- * 1: stage-2 positions that took it, 2: residual passes over V).  They are
+ * kernels increment (0: stage-1 tiles that took the exact radix-select
+ * fallback, 1: stage-2 positions with more segment lists than the call's
+ * shared memory holds (reported SS_ST_BAD_PARAM; not expected), 2: residual
+ * passes over V, 3: stage-1 CTAs that gave up waiting for a copy (their
+ * positions are left without candidates; not expected)).  They are
  * cumulative and only cleared by the caller. */
 size_t ss_workspace_diag_offset(const ss_plan* plan);
 

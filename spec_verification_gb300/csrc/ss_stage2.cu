@@ -500,7 +500,8 @@ __global__ void __launch_bounds__(kNT2, 9) stage2_kernel(const Params P, int ver
         P.out.tokens[r] = token;
         P.out.row_status[r] = status;
       }
-    } else if (warp == 0) {
+    } else if (warp == 0 && c0 + gamma + r < P.max_positions) {
+      // (a row whose positions reach past max_positions is reported below)
       if (lane == 0) {
         PosResult pr;
         pr.lse = lse;
@@ -569,6 +570,19 @@ __global__ void __launch_bounds__(kNT2, 9) stage2_kernel(const Params P, int ver
       }
     }
     __syncthreads();
+  }
+
+  // A verification batch with more target positions than the plan holds:
+  // the positions past max_positions were not evaluated, and a row reaching
+  // past it was neither counted nor walked, so it is reported here.
+  if (verify && __ldg(P.cu_draft + P.B) + P.B > P.max_positions) {
+    for (int r = blockIdx.x * kNT2 + tid; r < P.B; r += gridDim.x * kNT2) {
+      if (__ldg(P.cu_draft + r + 1) + r < P.max_positions) continue;
+      int32_t* tk = P.out.tokens + (size_t)r * P.out.tokens_stride;
+      for (int s = 0; s < P.out.tokens_stride; ++s) tk[s] = -1;
+      if (P.out.num_accepted) P.out.num_accepted[r] = 0;
+      P.out.row_status[r] = SS_ST_CAPACITY;
+    }
   }
 }
 

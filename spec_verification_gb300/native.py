@@ -17,6 +17,8 @@ SS_F32, SS_BF16 = 0, 1
 STATUS = {0: "SS_OK", -1: "SS_ERR_ARG", -2: "SS_ERR_ALIGN", -3: "SS_ERR_UNSUPPORTED",
           -4: "SS_ERR_WORKSPACE", -5: "SS_ERR_CUDA"}
 K = 128
+# row_status bit of a verification row past the plan's max_positions (SS_ST_CAPACITY)
+ST_CAPACITY = 1 << 9
 
 # numpy layouts of the device-side structs (all 4-byte fields, no padding)
 ROW_DTYPE = np.dtype([("flags", "<u4"), ("temperature", "<f4"), ("top_p", "<f4"), ("min_p", "<f4"),

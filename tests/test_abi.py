@@ -56,6 +56,7 @@ def test_struct_layouts_match_header():
 
 
 def test_flag_values_agree():
+    from spec_verification_gb300 import native
     from spec_verification_gb300 import workloads as W
     text = HEADER.read_text()
     for name, val in [("SS_GREEDY", W.GREEDY), ("SS_MASK", W.MASK), ("SS_PENALTY", W.PENALTY),
@@ -63,6 +64,8 @@ def test_flag_values_agree():
                       ("SS_BOUNDED_P", W.BOUNDED_P), ("SS_EXACT", W.EXACT)]:
         m = re.search(name + r" = 1u << (\d+)", text)
         assert m and (1 << int(m.group(1))) == val, name
+    m = re.search(r"SS_ST_CAPACITY = 1u << (\d+)", text)
+    assert m and (1 << int(m.group(1))) == native.ST_CAPACITY
 
 
 def test_plan_create_without_gpu_reports_error(lib):

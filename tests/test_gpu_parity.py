@@ -318,6 +318,41 @@ def test_verify_edge_cases():
     check(w)
 
 
+def test_verify_beyond_max_positions():
+    """cu_draft[B] + B is device data and may exceed the plan's max_positions:
+    the rows whose positions all fit are verified as usual, the others report
+    SS_ST_CAPACITY with no tokens, and the workspace counters stay clean for
+    the next call on the same workspace."""
+    from spec_verification_gb300 import native
+    from spec_verification_gb300.runner import DeviceRun
+    # positions: row 0 0-2, row 1 3-4, row 2 5-8, row 3 9-11, row 4 12, row 5 13-14
+    w = W.verify_workload(44, 6, 20000, [2, 1, 3, 2, 0, 1], dtype="f32", q_dtype="f32", truncation=True)
+    cap = 10  # row 3 straddles the bound: its position 9 is evaluated, 10 and 11 are not
+    d = DeviceRun(w, max_positions=cap)
+    d()
+    gpu = d.results()
+    fit = [0, 1, 2]
+    sub = subset(w, fit)
+    g = gpu_rows_as(gpu, w, fit)
+    rep = parity.compare_verify(sub, g, O.verify(sub, tokens_stride=gpu["tokens"].shape[1]))
+    assert rep.ok(), rep
+    for r in (3, 4, 5):
+        assert gpu["row_status"][r] == native.ST_CAPACITY
+        assert gpu["num_accepted"][r] == 0 and np.all(gpu["tokens"][r] == -1)
+    # the same plan and workspace for a batch that fits, whose row 3 is the
+    # straddling row above: a counter left behind would break its walk
+    w2 = subset(w, [0, 1, 4, 3])
+    w2.meta.pop("row_ids")  # a batch of its own: random streams keyed by its own rows
+    d2 = DeviceRun(w2, max_positions=cap)
+    d2.plan, d2.workspace = d.plan, d.workspace
+    for _ in range(2):
+        d2()
+        gpu2 = d2.results()
+        rep = parity.compare_verify(w2, gpu2, O.verify(w2, tokens_stride=gpu2["tokens"].shape[1]))
+        assert rep.ok(), rep
+        assert not np.any(gpu2["row_status"] & native.ST_CAPACITY)
+
+
 # ------------------------------------------------------------------ full-size workloads (sampled rows)
 
 def _sampled_full(w, n_rows, seed, tile=0):
