@@ -146,7 +146,8 @@ typedef struct {
   int64_t ld_logits;               /* row stride of the logits in elements (>= V) */
   int64_t ld_q;                    /* row stride of draft_probs in elements (>= V) */
   const ss_row_params* rows;       /* [B] */
-  const int32_t* cu_draft;         /* verify: [B+1] prefix sums of gamma_r, cu_draft[0] = 0 */
+  const int32_t* cu_draft;         /* verify: [B+1] prefix sums of gamma_r, cu_draft[0] = 0
+                                      (non-decreasing; not checked: other values are undefined) */
   int32_t hist_stride;             /* ints per history row (>= 1) */
   int32_t bias_stride;             /* entries per bias row (>= 1) */
   /* ss_verify only (ss_sample takes these as arguments): */
@@ -220,9 +221,9 @@ ss_status ss_plan_enable_exact(ss_plan* plan, int enable);
 /* Single-step sampling (SonicSampler 3.1-3.2; dl-note Combination).
  * logits:  [B, ld_logits] fp32 or bf16 (plan dtype), rows 16-byte aligned.
  * params:  host batch description (B, rows, strides, workspace, stream, plan).
- * history: [B, hist_stride] int32 or NULL (needed by rows with SS_PENALTY).
- * bitmask: [B, ceil(V/32)] uint32 or NULL (needed by rows with SS_MASK).
- * bias:    [B, bias_stride] ss_bias_entry or NULL (needed by rows with SS_BIAS).
+ * history: [B, hist_stride] int32 or NULL; with NULL, SS_PENALTY is ignored.
+ * bitmask: [B, ceil(V/32)] uint32 or NULL; with NULL, SS_MASK is ignored.
+ * bias:    [B, bias_stride] ss_bias_entry or NULL; with NULL, SS_BIAS is ignored.
  * seeds:   [B] uint64 Philox keys.
  * out:     host struct of device outputs: tokens [B], row_status [B], and the
  *          optional candidate outputs indexed by row.
@@ -245,7 +246,9 @@ ss_status ss_sample(const void* logits, const ss_batch* params, const int32_t* h
  *                case).  ld_q is ignored then.
  * draft_ids:     [cu_draft[B]] int32.
  * params:        as for ss_sample, plus cu_draft and the processor inputs
- *                history / bitmask (per target position) / bias.
+ *                history / bitmask (per target position) / bias, each NULL
+ *                or not as for ss_sample (a NULL history also leaves the
+ *                drafts uncounted: SS_PENALTY is ignored).
  * seeds:         [B] uint64.
  * out:           tokens [B, tokens_stride] (accepted drafts, then the
  *                resampled or bonus token, then -1), num_accepted [B],
