@@ -15,7 +15,8 @@ inputs already resident in HBM (the last G calls carry per-kernel events,
 which give the kernel durations of the roofline); `e2e` is the same metric with each step's
 inputs copied from pinned host memory and its tokens copied back inside the
 timed region.  Under torchrun each rank runs its own batch (weak scaling,
-no collective on the data path).  `--impl reference` times the CPU oracle.
+no collective on the data path).  `--impl reference` times the CPU oracle
+on every host core (one row per core per step).
 """
 from __future__ import annotations
 
