@@ -612,6 +612,20 @@ def test_mass_outside_top128_report():
     assert m[2] > 0.9 and m[3] > 0.9          # near-flat rows: nearly all mass outside
 
 
+def test_oracle_calls_are_independent_across_threads():
+    """The all-cores CPU baseline calls the oracle from several threads at
+    once: each call must give what it gives alone."""
+    import concurrent.futures as cf
+    w = W.mixed_workload(45, 12, 20000, "f32")
+    subs = [W.subset(w, [r]) for r in range(w.B)]
+    serial = [O.verify(s) for s in subs]
+    with cf.ThreadPoolExecutor(max_workers=6) as ex:
+        par = list(ex.map(O.verify, subs))
+    for a, b in zip(serial, par):
+        for k in ("tokens", "num_accepted", "row_status", "cand_ids", "cand_probs", "num_kept"):
+            assert np.array_equal(a[k], b[k]), k
+
+
 def test_packed16_staging_report():
     """The 16-bit-key report's full-precision side is the oracle's candidate
     set; its packed side loses exactly the two things a 16-bit key beside a
