@@ -16,7 +16,7 @@ which give the kernel durations of the roofline); `e2e` is the same metric with 
 inputs copied from pinned host memory and its tokens copied back inside the
 timed region.  Under torchrun each rank runs its own batch (weak scaling,
 no collective on the data path).  `--impl reference` times the CPU oracle
-on every host core (one row per core per step).
+on every host core (four rows per core per step).
 """
 from __future__ import annotations
 
@@ -248,32 +248,28 @@ class RowSubsets:
 
 
 def oracle_rows_parallel(subs, cores: int, budget_s: float | None = None, ex=None):
-    """The oracle, as it stands, on the one-row workloads `subs` partitioned
-    over `cores` threads: thread k takes subs[k], subs[k + cores], ... and
-    calls the single-threaded oracle on each (a ctypes call, which releases
-    the GIL).  With budget_s a thread starts no row after that many seconds.
-    Returns (rows done, target positions done, wall seconds)."""
+    """The oracle, as it stands, on the one-row workloads `subs` over `cores`
+    threads pulling rows from one queue in the given order; each thread calls
+    the single-threaded oracle (a ctypes call, which releases the GIL).  With
+    budget_s no row starts after that many seconds.  Returns (rows done,
+    target positions done, wall seconds)."""
     import concurrent.futures as cf
     from oracle import oracle
     oracle.lib()
     t0 = time.perf_counter()
 
-    def worker(k):
-        n = npos = 0
-        for i in range(k, len(subs), cores):
-            if budget_s is not None and time.perf_counter() - t0 >= budget_s:
-                break
-            s = subs[i]
-            (oracle.verify if s.is_verify else oracle.sample)(s)
-            n += 1
-            npos += s.n_positions
-        return n, npos
+    def one(i):
+        if budget_s is not None and time.perf_counter() - t0 >= budget_s:
+            return 0, 0
+        s = subs[i]
+        (oracle.verify if s.is_verify else oracle.sample)(s)
+        return 1, s.n_positions
 
     if ex is None:
         with cf.ThreadPoolExecutor(max_workers=cores) as own:
-            res = list(own.map(worker, range(cores)))
+            res = list(own.map(one, range(len(subs))))
     else:
-        res = list(ex.map(worker, range(cores)))
+        res = list(ex.map(one, range(len(subs))))
     return sum(a for a, _ in res), sum(b for _, b in res), time.perf_counter() - t0
 
 
@@ -304,8 +300,8 @@ def cpu_baseline(w, desc_name: str, budget_s: float = 12.0) -> dict:
             "sample": f"first {done_rows} rows ({npos} target positions) of {desc_name}, oracle bounded "
                       f"k=128 mode, single-threaded, {t_total:.1f} s",
             "all_cores": {"value": n_all / wall, "unit": "rows/s", "cores": cores,
-                          "sample": f"{n_all} rows ({npos_all} target positions) of {desc_name}, row r on "
-                                    f"thread r mod {cores}, {wall:.1f} s wall"}}
+                          "sample": f"{n_all} rows ({npos_all} target positions) of {desc_name} pulled by "
+                                    f"{cores} threads from one queue, {wall:.1f} s wall"}}
 
 
 def run_reference(args, w, desc):
@@ -320,9 +316,14 @@ def run_reference(args, w, desc):
     n_rows = min(w.B, 64)
     subs = [subset(w, [r]) for r in range(n_rows)]
 
+    per_step = 4 * cores
+
     def step(i, ex):
-        # one row per host core, in parallel, cycling over the first n_rows rows
-        oracle_rows_parallel([subs[(i * cores + k) % n_rows] for k in range(cores)], cores, ex=ex)
+        # four rows per host core, cycling over the first n_rows rows, pulled
+        # from one queue longest first so that no core idles behind a long row
+        rows = [subs[(i * per_step + k) % n_rows] for k in range(per_step)]
+        rows.sort(key=lambda s: -s.n_positions)
+        oracle_rows_parallel(rows, cores, ex=ex)
 
     with cf.ThreadPoolExecutor(max_workers=cores) as ex:
         for i in range(args.warmup):
@@ -331,10 +332,10 @@ def run_reference(args, w, desc):
         for i in range(args.steps):
             step(args.warmup + i, ex)
         dt = time.perf_counter() - t0
-    value = args.steps * cores / dt
-    sample = (f"{cores} rows (all their target positions) of {args.workload} per step, one per host "
-              f"core, cycling over the first {n_rows} rows; oracle bounded k=128 mode, single-threaded "
-              f"per row")
+    value = args.steps * per_step / dt
+    sample = (f"{per_step} rows (all their target positions) of {args.workload} per step on {cores} host "
+              f"cores (one queue, longest row first), cycling over the first {n_rows} rows; oracle bounded "
+              f"k=128 mode, single-threaded per row")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
