@@ -78,9 +78,8 @@ def library() -> C.CDLL:
     L.ss_plan_num_tiles.restype = C.c_int32
     L.ss_plan_stage1_ctas.argtypes = [C.c_void_p]
     L.ss_plan_stage1_ctas.restype = C.c_int32
-    if hasattr(L, "ss_plan_enable_exact"):
-        L.ss_plan_enable_exact.argtypes = [C.c_void_p, C.c_int]
-        L.ss_plan_enable_exact.restype = C.c_int
+    L.ss_plan_enable_exact.argtypes = [C.c_void_p, C.c_int]
+    L.ss_plan_enable_exact.restype = C.c_int
     L.ss_sample.argtypes = [C.c_void_p, C.POINTER(Batch), C.c_void_p, C.c_void_p, C.c_void_p,
                             C.c_void_p, C.POINTER(Out)]
     L.ss_sample.restype = C.c_int

@@ -88,3 +88,43 @@ def test_product_package_never_imports_oracle():
                 assert (node.module or "").split(".")[0] != "oracle", f
     for f in (pkg / "csrc").glob("*"):
         assert not re.search(r"\bsso_|oracle/|liboracle", f.read_text()), f
+
+
+def test_host_side_misuse_returns_negative_codes(lib):
+    """Arguments the host can check are refused before any device query or
+    launch, with the header's negative status codes."""
+    import ctypes as C
+    from spec_verification_gb300 import native
+    L = native.library()
+    ERR_ARG, ERR_UNSUPPORTED = -1, -3
+    p = C.c_void_p(12345)
+
+    def create(V=1000, rows=4, positions=8, ldt=0, qdt=0, tile=0):
+        p.value = 12345
+        return L.ss_plan_create(C.byref(p), V, rows, positions, ldt, qdt, tile, 0)
+
+    for kw, code in [({"V": 0}, ERR_UNSUPPORTED), ({"V": (1 << 20) + 1}, ERR_UNSUPPORTED),
+                     ({"rows": 0}, ERR_ARG), ({"positions": 3}, ERR_ARG),
+                     ({"positions": (1 << 24) + 1}, ERR_ARG), ({"ldt": 7}, ERR_ARG),
+                     ({"qdt": -1}, ERR_ARG), ({"tile": 4096}, ERR_UNSUPPORTED)]:
+        assert create(**kw) == code, kw
+        assert p.value is None, kw          # *plan is NULL on failure
+        assert L.ss_last_error()             # and the reason is recorded
+    assert L.ss_plan_create(None, 1000, 4, 8, 0, 0, 0, 0) == ERR_ARG
+    # calls without params, out or plan
+    out = native.Out()
+    batch = native.Batch()
+    assert L.ss_sample(None, None, None, None, None, None, C.byref(out)) == ERR_ARG
+    assert L.ss_sample(None, C.byref(batch), None, None, None, None, None) == ERR_ARG
+    assert L.ss_sample(None, C.byref(batch), None, None, None, None, C.byref(out)) == ERR_ARG
+    assert L.ss_verify(None, None, None, C.byref(batch), None, C.byref(out)) == ERR_ARG
+    assert L.ss_sample_noalloc(None, C.byref(batch), None, None, None, None, C.byref(out)) == ERR_ARG
+    assert L.ss_plan_enable_exact(None, 1) == ERR_ARG
+    # plan queries on NULL
+    assert L.ss_workspace_bytes(None) == 0 and L.ss_plan_tile(None) == 0
+    assert L.ss_plan_num_tiles(None) == 0 and L.ss_plan_stage1_ctas(None) == 0
+    L.ss_plan_destroy(None)
+    for code, text in [(0, b"ok"), (-1, b"invalid argument"), (-2, b"misaligned row"),
+                       (-3, b"unsupported size"), (-4, b"workspace too small"), (-5, b"CUDA error"),
+                       (42, b"unknown status")]:
+        assert L.ss_status_str(code) == text
