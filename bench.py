@@ -349,6 +349,24 @@ def run_reference(args, w, desc):
     print(json.dumps(line), flush=True)
 
 
+def input_copies(call_bytes: int, l2_bytes: int, G: int) -> int:
+    """Resident copies of a call's streamed inputs (logits, draft probs) so
+    that consecutive passes over them hold at least twice the L2 size: 2
+    when two copies already do, else the next multiple of the G calls per
+    graph."""
+    need = max(2, -(-2 * l2_bytes // max(1, call_bytes)))
+    return 2 if need <= 2 else -(-need // G) * G
+
+
+def graph_copies(R: int, G: int) -> list:
+    """The copy each call of each captured graph uses: call i of graph j
+    takes copy (j * G + i) mod R, so replaying the R / gcd(R, G) graphs in
+    turn walks through every copy in order."""
+    import math
+    NG = R // math.gcd(R, G)
+    return [[(j * G + i) % R for i in range(G)] for j in range(NG)]
+
+
 def run_ours(args, w, desc):
     import torch
     import torch.distributed as dist
@@ -364,10 +382,19 @@ def run_ours(args, w, desc):
     run = DeviceRun(w, device=str(dev), candidates=False, tile=args.tile)
     verify = w.is_verify
     K, Wm = args.steps, args.warmup
-    # two resident copies of the large inputs, alternated between steps
-    lg = [run.d["logits"], run.d["logits"].clone()]
-    qq = [run.d.get("draft_probs"), run.d["draft_probs"].clone() if "draft_probs" in run.d else None]
     G = max(d for d in range(1, min(10, K) + 1) if K % d == 0)
+    # resident copies of the streamed inputs, walked in turn so that nothing
+    # is served from L2 (together at least twice its size)
+    call_bytes = sum(t.numel() * t.element_size() for t in (run.d["logits"], run.d.get("draft_probs"))
+                     if t is not None)
+    l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or (129 << 20))
+    R = input_copies(call_bytes, l2, G)
+    lg = [run.d["logits"]] + [run.d["logits"].clone() for _ in range(R - 1)]
+    qq = [run.d.get("draft_probs")] + [run.d["draft_probs"].clone() if "draft_probs" in run.d else None
+                                       for _ in range(R - 1)]
+    plan = graph_copies(R, G)
+    NG = len(plan)
+    j_ev = (K // G - 1) % NG  # the timed region's last replay, the one with events
     stream = torch.cuda.Stream(device=dev)
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(G)]
     for row in ev:  # torch creates the underlying cudaEvent_t at the first record
@@ -377,22 +404,26 @@ def run_ours(args, w, desc):
         for i in range(2):
             run(logits=lg[i % 2], draft_probs=qq[i % 2])
     stream.synchronize()
-    # Two graphs of the same G calls: `graph` without instrumentation, and
-    # `graph_ev` with an event before, between and after the kernels of each
-    # call.  Event nodes cost about 15 us per call here, so the timed region
-    # replays `graph` for all but its last G calls, which come from `graph_ev`
-    # and give the per-kernel durations (measured inside the timed region).
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=stream):
-        for i in range(G):
-            run(logits=lg[i % 2], draft_probs=qq[i % 2])
+    # Graphs of G calls: one per set of copies in `graphs`, without
+    # instrumentation, and `graph_ev` with an event before, between and after
+    # the kernels of each call.  Event nodes cost about 15 us per call here,
+    # so the timed region replays `graphs` in turn for all but its last G
+    # calls, which come from `graph_ev` (on the copies next in turn) and give
+    # the per-kernel durations (measured inside the timed region).
+    graphs = []
+    for cp in plan:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(G):
+                run(logits=lg[cp[i]], draft_probs=qq[cp[i]])
+        graphs.append(g)
     graph_ev = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph_ev, stream=stream):
         for i in range(G):
-            run(logits=lg[i % 2], draft_probs=qq[i % 2], events=ev[i])
+            run(logits=lg[plan[j_ev][i]], draft_probs=qq[plan[j_ev][i]], events=ev[i])
     with torch.cuda.stream(stream):
-        for _ in range(max(1, -(-Wm // G))):
-            graph.replay()
+        for t in range(max(1, -(-Wm // G))):
+            graphs[t % NG].replay()
         graph_ev.replay()
     stream.synchronize()
 
@@ -406,8 +437,8 @@ def run_ours(args, w, desc):
     t_end = torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         t_start.record(stream)
-        for _ in range(K // G - 1):
-            graph.replay()
+        for t in range(K // G - 1):
+            graphs[t % NG].replay()
         graph_ev.replay()
         t_end.record(stream)
     torch.cuda.synchronize(dev)
@@ -477,8 +508,10 @@ def run_ours(args, w, desc):
             "dtype": "f32" if w.dtype == "f32" else "bf16", "data": "synthetic",
             "config": {"workload": desc, "name": args.workload, "B": w.B, "V": w.V,
                        "positions": w.n_positions, "tile": tile, "tiles_per_row": run.plan.num_tiles,
-                       "l2": "inputs larger than L2 (two resident copies alternated)",
-                       "graph": f"{G} calls per CUDA graph, {K // G} replays, the last with per-kernel events", "parallelism": f"replicas{world}"},
+                       "l2": f"inputs larger than L2: {R} resident copies walked in turn "
+                             f"({R * call_bytes / 1e6:.0f} MB against {l2 / 1e6:.0f} MB of L2)",
+                       "graph": f"{G} calls per CUDA graph ({NG} graphs over the copies), {K // G} replays, "
+                                f"the last with per-kernel events", "parallelism": f"replicas{world}"},
             "roofline": {"bound": "hbm", "kernel": "stage1", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_kind": peak_kind,
                          "traffic": traffic, "alg_bytes_per_launch": alg1},
