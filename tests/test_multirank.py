@@ -34,7 +34,7 @@ def _rank(rank, world, port, times, out):
 def test_two_gloo_ranks_take_the_slowest_time():
     world, port = 2, _free_port()
     times = [3.5, 7.25]
-    out = mp.Manager().dict()
+    out = mp.get_context("spawn").Manager().dict()  # no fork of this (threaded) process
     mp.spawn(_rank, args=(world, port, times, out), nprocs=world, join=True)
     for r in range(world):
         ms, rate = out[r]
