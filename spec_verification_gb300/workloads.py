@@ -11,7 +11,7 @@ on.
 The pages measure on logits of trained LLMs, which are not available here; the
 generators below stand in for them.  The structure follows the SonicSampler
 page (low-entropy next-token distributions, vocabularies of 2^17..2^18 tokens,
-section 1) and the five workload descriptions of the benchmark spec:
+section 1) in five standard workloads:
 
   c1  single-step, B=4, V=32000 fp32 N(0,2) plus five spike tokens +8..+12
   c2  single-step heterogeneous, B=64, V=131072 bf16, all processors
@@ -101,7 +101,7 @@ class Workload:
         return self.logits.nbytes
 
     def counted_bytes(self, tile: int) -> int:
-        """Bytes the benchmark spec's metric counts per call: logits + bitmask +
+        """Bytes the throughput metric counts per call: logits + bitmask +
         draft probs (read once) + staging write and read (128 entries of 8
         bytes per vocab tile)."""
         z = -(-self.V // tile)
