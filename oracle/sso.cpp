@@ -25,7 +25,7 @@
 //  [PX]  Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy as
 //        1, 2, 3", SC'11 -- Philox-4x32 with 10 rounds.
 //
-// Readings where the pages are silent (each is listed in the design notes):
+// Readings where the pages are silent:
 //  - penalty formulas (the paper's appendix C is missing): CTRL repetition
 //    penalty x/rep for x > 0 else x*rep, then x - freq*count, then x - pres,
 //    applied only to tokens with count > 0;
