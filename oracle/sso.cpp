@@ -29,8 +29,9 @@
 //  - penalty formulas (the paper's appendix C is missing): CTRL repetition
 //    penalty x/rep for x > 0 else x*rep, then x - freq*count, then x - pres,
 //    applied only to tokens with count > 0;
-//  - temperature is applied as a multiplication by the fp32 reciprocal
-//    RN(1/T); greedy rows skip temperature and truncation;
+//  - temperature divides each logit by T ([DN] Temperature: z_i / T), one
+//    IEEE fp32 division rounded to nearest; greedy rows skip temperature and
+//    truncation;
 //  - the order is (processed logit descending, token index ascending); NaN
 //    after the prelude becomes -inf and sets a status bit; -0 == +0;
 //  - bounded mode: the candidate universe is the first min(128, V) tokens of
@@ -269,10 +270,10 @@ std::vector<float> prelude(const sso_problem& P, int r, int64_t pos, const std::
       x[t] = x[t] + P.bias_values[(int64_t)r * P.bias_stride + e];
     }
   }
-  // 4. temperature (stochastic rows only): x * RN(1/T).
+  // 4. temperature (stochastic rows only): x / T, one fp32 division.
   if (!(rp.flags & kGreedy)) {
-    const float rt = 1.0f / rp.temperature;
-    for (int i = 0; i < V; ++i) x[i] = x[i] * rt;
+    const float T = rp.temperature;
+    for (int i = 0; i < V; ++i) x[i] = x[i] / T;
   }
   // 5. NaN -> -inf.
   for (int i = 0; i < V; ++i)

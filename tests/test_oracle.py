@@ -661,3 +661,203 @@ def test_config1_reference_behaviour():
     assert out["tokens"][0] == int(np.argmax(x[0])) and out["tokens"][1] == int(np.argmax(x[1]))
     assert np.all(out["num_kept"][2:] <= 50)
     assert np.all(out["row_status"] == 0)
+
+
+# ----------------------------------------------------------------------------- temperature as division
+
+def _nearest_f32(num):
+    """The fp32 value nearest to the rational `num` (ties to the even
+    significand), found from the exact rational by bracketing, independent of
+    any floating-point division."""
+    from fractions import Fraction
+    limit = Fraction(2 ** 128) - Fraction(2 ** 103)   # FLT_MAX + half an ulp: rounds to infinity
+    if abs(num) >= limit:
+        return np.float32(np.inf) if num > 0 else np.float32(-np.inf)
+    f = np.float32(float(num))          # within an ulp or two of the answer
+    cands = [f]
+    for _ in range(3):
+        cands.append(np.nextafter(cands[-1], np.float32(np.inf)))
+    g = f
+    for _ in range(3):
+        g = np.nextafter(g, np.float32(-np.inf))
+        cands.append(g)
+    best = min(cands, key=lambda c: (abs(Fraction(float(c)) - num),
+                                     int(np.array(c, np.float32).view(np.uint32)) & 1))
+    return best
+
+
+def test_temperature_is_one_correctly_rounded_division():
+    """dl-note, Temperature: the processed logit is z / T.  Each processed
+    value must be the fp32 number nearest the exact quotient (IEEE division,
+    round to nearest even), checked with exact rational arithmetic; the
+    reciprocal form z * RN(1/T) is a different function and is caught."""
+    from fractions import Fraction
+    rng = np.random.default_rng(71)
+    x = np.concatenate([rng.standard_normal(600) * 4, rng.standard_normal(100) * 1e-3,
+                        [0.0, -0.0, 1e-38, -3e38, 7.0, -np.inf]]).astype(np.float32)[None]
+    differs = 0
+    for T in (0.37, 0.7, 1.3, 2.9, 0.5123):
+        T32 = np.float32(T)
+        got, _ = _processed(sample_case(x, flags=0, temperature=T32))
+        with np.errstate(over="ignore"):
+            recip = (x[0] * np.float32(np.float32(1.0) / T32)).astype(np.float32)
+        for i, v in enumerate(x[0]):
+            if not np.isfinite(v):
+                assert got[i] == v
+                continue
+            want = _nearest_f32(Fraction(float(v)) / Fraction(float(T32)))
+            assert got[i] == want, (T, i, v, got[i], want)
+        differs += int(np.sum(recip != got))
+    assert differs > 0
+
+
+# ----------------------------------------------------------------------------- margins (parity diagnostics)
+
+def _g32(seed, i, position, row, purpose):
+    """Gumbel noise -ln(-ln u) from the pinned uniform, in fp32 steps."""
+    u = np.float32(O.uniform(seed, i, position, row, purpose))
+    return np.float32(-np.log(np.float32(-np.log(u))))
+
+
+def test_margin_gumbel_is_relative_gap_of_the_two_best_scores():
+    """The Gumbel-argmax margin is (s_1 - s_2) / |s_1| for the two best
+    perturbed scores s = l + g: build rows whose two best scores are a chosen
+    gap apart and check the reported margin and the winner."""
+    seed = 12345
+    g = [_g32(seed, i, 0, 0, 0) for i in range(3)]
+    for gap in (3e-6, 2e-4, 0.5):
+        l = np.zeros((1, 3), np.float32)
+        l[0, 0] = np.float32(2.0) - g[0]
+        l[0, 1] = np.float32(2.0 + gap) - g[1]
+        l[0, 2] = np.float32(-30.0)
+        w = sample_case(l, flags=0, seeds=[seed])
+        out = O.sample(w)
+        s = np.array([np.float32(l[0, i] + g[i]) for i in range(3)], np.float64)
+        order = np.argsort(-s, kind="stable")
+        want = (s[order[0]] - s[order[1]]) / abs(s[order[0]])
+        assert int(out["tokens"][0]) == int(order[0])
+        np.testing.assert_allclose(out["margin_gumbel"][0], want, rtol=1e-3)
+        assert 0.5 * gap / 2.0 < out["margin_gumbel"][0] < 2.0 * gap / 2.0
+    # one kept token (top-k = 1) and greedy rows decide nothing by noise
+    x = np.array([[1.0, 0.5, 0.25]], np.float32)
+    assert np.isinf(O.sample(sample_case(x, flags=F.TOPK, top_k=1))["margin_gumbel"][0])
+    assert np.isinf(O.sample(sample_case(x, flags=F.GREEDY))["margin_gumbel"][0])
+
+
+def test_margin_topp_is_distance_of_cumulative_mass_to_top_p():
+    """The top-p margin is the smallest |mass before t - top_p| over the
+    candidates (and the full mass): a top_p placed 1e-7 above and below the
+    mass of the first two tokens gives that distance and keeps 3 or 2."""
+    l = np.log(np.array([0.5, 0.3, 0.2])).astype(np.float32)[None]
+    p = _softmax64(l[0])
+    c2 = p[0] + p[1]
+    for delta, keep in ((1e-7, 3), (-1e-7, 2)):
+        tp = np.float32(c2 + delta)
+        out = O.sample(sample_case(l, flags=F.TOPP, top_p=tp))
+        cums = [0.0, p[0], c2, 1.0]
+        want = min(abs(c - float(tp)) for c in cums)
+        np.testing.assert_allclose(out["margin_topp"][0], want, rtol=1e-6)
+        assert 3e-8 < out["margin_topp"][0] < 2e-7
+        assert int(out["num_kept"][0]) == keep
+    assert np.isinf(O.sample(sample_case(l, flags=0))["margin_topp"][0])
+
+
+def test_margin_minp_is_distance_to_log_min_p():
+    """The min-p margin is the smallest |(l_t - l_0) - ln(min_p)| over finite
+    candidates (logit-space rule)."""
+    l = np.array([[0.0, -1.0, -2.3, -np.inf]], np.float32)
+    for mp, keep in ((0.1003, 2), (0.1002, 3)):
+        mp32 = np.float32(mp)
+        out = O.sample(sample_case(l, flags=F.MINP, min_p=mp32))
+        thr = np.log(np.float64(mp32))
+        want = min(abs(float(v) - thr) for v in l[0] if np.isfinite(v))
+        np.testing.assert_allclose(out["margin_minp"][0], want, rtol=1e-9)
+        assert int(out["num_kept"][0]) == keep
+
+
+def test_margin_accept_is_relative_distance_of_u_q_to_p():
+    """Verification margin |fp32(u q(d)) - p(d)| / p(d), with u the pinned
+    acceptance uniform; q(d) is set so that u q(d) lands a chosen relative
+    distance from p(d), on both sides of the accept rule."""
+    V = 4
+    l = np.array([0.7, 0.1, -0.4, -1.0], np.float32)
+    p = _softmax64(l)
+    seed, d = 777, 1
+    u = np.float32(O.uniform(seed, 0, 0, 0, 1))
+    for rel, acc in ((3e-4, 0), (-3e-4, 1)):
+        qd = np.float32(p[d] * (1 + rel) / float(u))
+        q = np.full((1, V), (1 - float(qd)) / (V - 1), np.float32)
+        q[0, d] = qd
+        w = verify_case(np.stack([l, l]), q, [d], [1], seeds=[seed])
+        out = O.verify(w)
+        prod = float(np.float32(u * qd))
+        want = abs(prod - p[d]) / p[d]
+        np.testing.assert_allclose(out["margin_accept"][0], want, rtol=1e-6)
+        assert 1e-4 < out["margin_accept"][0] < 1e-3
+        assert int(out["num_accepted"][0]) == acc
+        np.testing.assert_allclose(out["p_draft"][0], p[d], rtol=1e-12)
+
+
+def test_margin_resid_is_relative_gap_of_residual_scores():
+    """After a rejection the residual token is the argmax of ln r_i + g_i
+    (purpose 2) over r_i = max(0, p_i - q_i) > 0; the margin is the relative
+    gap of its two best scores."""
+    V = 4
+    l = np.array([1.0, 0.9, -3.0, -3.0], np.float32)
+    p = _softmax64(l)
+    seed = 4242
+    q = np.array([[0.0, 0.0, 0.5, 0.5]], np.float32)  # draft 2: p(2) small, u q(2) > p(2) -> reject
+    w = verify_case(np.stack([l, l]), q, [2], [1], seeds=[seed])
+    u = np.float32(O.uniform(seed, 0, 0, 0, 1))
+    assert float(np.float32(u * np.float32(0.5))) > p[2]
+    out = O.verify(w)
+    assert int(out["num_accepted"][0]) == 0
+    r = np.maximum(0.0, p - q[0].astype(np.float64))
+    s = {i: np.float32(np.log(np.float32(r[i])) + _g32(seed, i, 0, 0, 2)) for i in range(V) if r[i] > 0}
+    best = sorted(s.items(), key=lambda kv: (-float(kv[1]), kv[0]))
+    assert int(out["tokens"][0, 0]) == best[0][0]
+    want = (float(best[0][1]) - float(best[1][1])) / abs(float(best[0][1]))
+    np.testing.assert_allclose(out["margin_resid"][0], want, rtol=1e-3)
+
+
+# ----------------------------------------------------------------------------- empty residual
+
+def test_empty_residual_draws_from_p_with_status():
+    """q >= p everywhere (a bf16-rounded q can sum above 1): max(0, p - q) has
+    no mass, so a rejection draws from p itself and reports the empty
+    residual.  Acceptance is min(1, p(d)/q(d)) = 0.8 for q = 1.25 p, and the
+    rejected rows' tokens are distributed as p."""
+    rng = np.random.default_rng(91)
+    V, B = 6, 30000
+    l = (rng.standard_normal(V) * 1.2).astype(np.float32)
+    p = _softmax64(l)
+    q = (1.25 * p).astype(np.float32)
+    assert np.all(q.astype(np.float64) > p)
+    w = _verify_stat_case(V, B, l, q, 1, 0, 13)
+    out = O.verify(w)
+    rej = out["num_accepted"] == 0
+    st = out["row_status"]
+    assert np.all((st[rej] & (1 << 7)) != 0) and np.all((st[~rej] & (1 << 7)) == 0)
+    acc = 1.0 - rej.mean()
+    assert abs(acc - 0.8) < 4 * np.sqrt(0.16 / B)
+    counts = np.bincount(out["tokens"][rej, 0], minlength=V)
+    assert chi2_pvalue(counts, p) > 1e-4
+
+
+# ----------------------------------------------------------------------------- outside-128 mass, closed form
+
+def test_mass_outside_closed_forms():
+    """1 - (full-softmax mass of the 128 candidates), against closed forms:
+    128 tokens at logit 0 and V - 128 at ln(eps) leave (V-128) eps / (128 +
+    (V-128) eps) outside; 300 equal logits leave 172/300."""
+    V = 1000
+    a = np.float32(np.log(1e-3))
+    x = np.full((1, V), a, np.float32)
+    x[0, 300:428] = 0.0
+    out = O.sample(sample_case(x, flags=0), exact=True)
+    e = np.exp(np.float64(a))
+    want = (V - 128) * e / (128 + (V - 128) * e)
+    np.testing.assert_allclose(out["mass_outside"][0], want, rtol=1e-9)
+    assert sorted(out["cand_ids"][0].tolist()) == list(range(300, 428))
+    out = O.sample(sample_case(np.zeros((1, 300), np.float32), flags=0), exact=True)
+    np.testing.assert_allclose(out["mass_outside"][0], 172 / 300, rtol=1e-12)
