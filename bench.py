@@ -523,10 +523,12 @@ def run_ours(args, w, desc):
             "clocks": ck,
             "e2e": e2e,
             "gpu_launches": K * (3 if verify else 2),
-            # stage-1 self-checks over every call of the run: stages resolved by
-            # the exact fallback, and bulk copies that did not land in time
+            # stage-1 counters over every call of the run: stages replaced by
+            # their exact top-128, candidate buffers cut back to their exact
+            # top-128, and bulk copies that did not land within the wait limit
             # (nonzero: the run's results are not valid)
-            "self_check": {"stage_fallbacks": int(diag[0]), "copy_timeouts": int(diag[3])},
+            "self_check": {"stage_fallbacks": int(diag[0]), "buffer_compactions": int(diag[4]),
+                           "copy_timeouts": int(diag[3])},
             "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)

@@ -34,7 +34,8 @@
  *    order: mask (bit i%32 of word i/32, 1 = allowed, else -inf); if count
  *    c of token i in the history is > 0 and SS_PENALTY: x = x>0 ? x/rep :
  *    x*rep, then x -= freq*c, then x -= pres; if SS_BIAS: each bias entry for
- *    token i is added in list order; stochastic rows: x *= RN(1/T); a NaN
+ *    token i is added in list order; stochastic rows: x /= T (one IEEE
+ *    division, dl-note Temperature); a NaN
  *    result becomes -inf (status SS_ST_NAN);
  *  - candidate order: processed logit descending, token id ascending (-0 and
  *    +0 are equal); candidates are the first min(128, V) tokens in that order;
@@ -109,9 +110,13 @@ enum {
   SS_ST_RESID_EMPTY = 1u << 7, /* residual max(0, p - q) had no mass: sampled from p */
   SS_ST_NOT_EXACT = 1u << 8,    /* SS_EXACT on a plan without exact sampling:
                                    sampled from the 128 candidates */
-  SS_ST_CAPACITY = 1u << 9      /* verification: the row's target positions reach
+  SS_ST_CAPACITY = 1u << 9,     /* verification: the row's target positions reach
                                    past the plan's max_positions; not verified,
                                    tokens -1, num_accepted 0 */
+  SS_ST_COPY_TIMEOUT = 1u << 10 /* a stage-1 copy of this row's logits did not
+                                   land within the wait limit: the row's result
+                                   is not valid (not expected; see
+                                   ss_plan_set_wait_limit) */
 };
 
 /* One row's sampling parameters (device array of B entries, 44 bytes each).
@@ -289,13 +294,33 @@ const char* ss_status_str(ss_status s);
 /* Text of the last error on the calling host thread ("" if none). */
 const char* ss_last_error(void);
 
+/* Wait limit of stage 1's copy ring: a thread polls a ring slot's
+ * completion at most `polls` times (0 restores the default, 2^22 polls)
+ * before it counts the copy as lost.  suspend_ns == 0 (the default): each
+ * poll may suspend the thread in hardware until the copy lands or the
+ * hardware's time limit passes (2^22 such polls of a copy that never lands
+ * take about 15 s).  suspend_ns > 0: each poll tests once without suspending
+ * and then sleeps about suspend_ns nanoseconds.  A CTA that gives up stops
+ * waiting, writes empty candidate lists with SS_ST_COPY_TIMEOUT for its
+ * remaining positions (so their rows report it), counts itself in
+ * diagnostic counter 3 and lets the copies it issued land (waiting up to
+ * 2^22 suspending polls for them) before it exits.  A lost copy is not
+ * expected: a short limit (one poll, suspend_ns = 1) is a way to exercise
+ * this path, since the copies still land, only later than the waits allow.
+ * Not thread-safe against calls using the plan.  Returns SS_ERR_ARG for a
+ * NULL plan. */
+ss_status ss_plan_set_wait_limit(ss_plan* plan, uint32_t polls, uint32_t suspend_ns);
+
 /* Byte offset, inside the workspace, of 8 uint32 diagnostic counters the
- * kernels increment (0: stage-1 tiles that took the exact radix-select
- * fallback, 1: stage-2 positions with more segment lists than the call's
- * shared memory holds (reported SS_ST_BAD_PARAM; not expected), 2: residual
- * passes over V, 3: stage-1 CTAs that gave up waiting for a copy (their
- * positions are left without candidates; not expected)).  They are
- * cumulative and only cleared by the caller. */
+ * kernels increment: 0: stage-1 stages replaced by their exact top-128 (the
+ * candidate buffer overflowed within the stage, or a segment's first stage
+ * certified fewer than 128 elements); 1: stage-2 positions with more segment
+ * lists than the call's shared memory holds (reported SS_ST_BAD_PARAM; not
+ * expected); 2: residual passes over V; 3: stage-1 CTAs that gave up
+ * waiting for a copy (their positions are left without candidates and
+ * report SS_ST_COPY_TIMEOUT; not expected); 4: stage-1 candidate buffers cut
+ * back to their exact top-128 after a histogram raise left too many.  They
+ * are cumulative and only cleared by the caller. */
 size_t ss_workspace_diag_offset(const ss_plan* plan);
 
 #ifdef __cplusplus

@@ -28,6 +28,8 @@ int residual_piece_tokens();
 struct ss_plan {
   int V, max_rows, max_positions, BN, Z, device, sms, nslot;
   int exact;  // stage 1 runs its exact-sampling variant
+  uint32_t spin_limit;  // polls of a stage-1 ring wait before it gives up
+  uint32_t spin_hint_ns;  // suspend-time hint of each poll (0: the hardware's)
   ss_dtype ldt, qdt;
   int grid1, grid2, grid3;
   std::vector<int> grid2_by_cap;  // stage-2 grid for a shared-memory capacity of c lists (index c)
@@ -39,6 +41,11 @@ struct ss_plan {
 namespace {
 
 thread_local std::string g_err;
+
+// Polls of a stage-1 ring wait before the copy counts as lost.  The hardware
+// suspends a polling thread between polls; measured, 2^22 polls of a copy
+// that never lands take about 15 s.
+constexpr uint32_t kDefaultSpin = 1u << 22;
 
 ss_status fail(ss_status s, const char* msg) {
   g_err = msg;
@@ -138,6 +145,8 @@ ss_status ss_plan_create(ss_plan** out, int32_t V, int32_t max_rows, int32_t max
   p->qdt = q_dtype;
   p->k1 = ss::stage1_ptr(bf16, false);
   p->exact = 0;
+  p->spin_limit = kDefaultSpin;
+  p->spin_hint_ns = 0u;
   p->smem1 = ss::stage1_smem_bytes(BN, bf16, nslot);
   p->smem2 = ss::stage2_smem_bytes(p->Z);
   p->smem3 = ss::residual_smem_bytes(BN);
@@ -220,6 +229,13 @@ ss_status ss_plan_enable_exact(ss_plan* p, int enable) {
 }
 size_t ss_workspace_diag_offset(const ss_plan* p) { return p ? p->off_diag : 0; }
 
+ss_status ss_plan_set_wait_limit(ss_plan* p, uint32_t polls, uint32_t suspend_ns) {
+  if (!p) return fail(SS_ERR_ARG, "plan is required");
+  p->spin_limit = polls == 0 ? kDefaultSpin : polls;
+  p->spin_hint_ns = suspend_ns;
+  return SS_OK;
+}
+
 }  // extern "C"
 
 namespace {
@@ -255,6 +271,8 @@ ss_status fill_common(const ss_plan* pl, const ss_batch* b, const void* logits, 
   P.max_positions = pl->max_positions;
   P.grid1 = pl->grid1;
   P.nslot = pl->nslot;
+  P.spin_limit = pl->spin_limit;
+  P.spin_hint_ns = pl->spin_hint_ns;
   char* w = static_cast<char*>(b->workspace);
   P.ws.staging = reinterpret_cast<unsigned long long*>(w + pl->off_staging);
   P.ws.tile_lse = reinterpret_cast<float2*>(w + pl->off_tlse);

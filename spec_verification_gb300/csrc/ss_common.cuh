@@ -72,6 +72,8 @@ struct Params {
   int seg_cap;              // segment lists per position that stage 2's shared memory holds
   int exact_on;             // the plan runs the exact-sampling variant of stage 1
   int mask_tma;             // bitmask rows can be bulk-copied (16-byte aligned rows)
+  uint32_t spin_limit;      // polls of a stage-1 ring wait before it gives up (the copy timeout)
+  uint32_t spin_hint_ns;    // suspend-time hint of each poll in ns (0: the hardware's limit)
   Workspace ws;
   ss_out out;
 };
@@ -135,7 +137,7 @@ __device__ __forceinline__ float gumbel_of(float u) { return -logf(-logf(u)); }
 // ------------------------------------------------------------------ row parameters
 struct RowCtx {
   uint32_t flags;
-  float rT, rep, freq, pres, top_p, min_p;
+  float T, rep, freq, pres, top_p, min_p;  // T: the temperature of stochastic rows (greedy: 1)
   int top_k, hist_len, n_bias;
   uint32_t position;
   bool valid, stoch, trunc;
@@ -166,7 +168,7 @@ __device__ __forceinline__ RowCtx make_row(const ss_row_params& p, int hist_stri
     if (p.flags & SS_TOPK) ok = ok && p.top_k >= 0;
   }
   c.valid = ok;
-  c.rT = c.stoch ? __fdiv_rn(1.0f, p.temperature) : 1.0f;
+  c.T = c.stoch ? p.temperature : 1.0f;
   // truncating rows (and SS_BOUNDED_P rows) verify against the kept candidate
   // distribution; the others against the softmax over the whole vocabulary
   const bool cuts = ((p.flags & SS_TOPK) && p.top_k > 0) || ((p.flags & SS_TOPP) && p.top_p < 1.0f) ||
@@ -174,6 +176,12 @@ __device__ __forceinline__ RowCtx make_row(const ss_row_params& p, int hist_stri
   c.trunc = c.stoch && (cuts || (p.flags & SS_BOUNDED_P));
   c.exact = c.stoch && !cuts && (p.flags & SS_EXACT);
   return c;
+}
+
+// Temperature (dl-note, Temperature: z / T): one IEEE fp32 division, rounded
+// to nearest, for stochastic rows; greedy rows keep the logit.
+__device__ __forceinline__ float apply_temperature(float x, const RowCtx& rc) {
+  return rc.stoch ? __fdiv_rn(x, rc.T) : x;
 }
 
 // Penalties and bias for one element whose history count is c (> 0 only for

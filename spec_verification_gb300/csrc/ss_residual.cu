@@ -45,7 +45,7 @@ __device__ __forceinline__ void prelude4(const Params& P, const RowCtx& rc, int 
       const uint32_t a = aux[i - t0];
       if (a != 0u) x = apply_penalty_bias(x, a & 0x7FFFu, (a & 0x8000u) != 0u, i, rc, brow);
     }
-    if (rc.stoch) x = __fmul_rn(x, rc.rT);
+    x = apply_temperature(x, rc);
     if (x != x) x = -INFINITY;
     out[k] = x;
   }

@@ -53,7 +53,7 @@ namespace ss {
 
 namespace {
 
-constexpr int kSpinLimit = 1 << 22;  // bounded mbarrier wait (about a second)
+constexpr uint32_t kDrainSpin = 1u << 22;  // polls of the final drain of copies in flight
 constexpr int kMaxSlots = 4;         // ring slots at most
 constexpr int kCap = 1024;           // candidate buffer entries
 constexpr int kRaiseAt = 384;        // buffer fill that triggers a cut raise
@@ -130,18 +130,37 @@ __device__ __forceinline__ void bulk_copy(void* dst, const void* src, uint32_t b
                : "memory");
 }
 
-__device__ __forceinline__ bool mbar_wait(unsigned long long* m, uint32_t parity) {
-  for (int i = 0; i < kSpinLimit; ++i) {
+// Waits for the phase of parity `parity` of mbarrier m to complete, polling
+// at most `limit` times; false if it did not.  hint_ns == 0: each poll may
+// suspend the thread in hardware until the phase completes or the hardware's
+// time limit passes.  hint_ns > 0: each poll tests once, without suspending,
+// and then sleeps about hint_ns nanoseconds.
+__device__ __forceinline__ bool mbar_wait(unsigned long long* m, uint32_t parity, uint32_t limit, uint32_t hint_ns) {
+  for (uint32_t i = 0; i < limit; ++i) {
     uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(ok)
-        : "r"(smem_u32(m)), "r"(parity)
-        : "memory");
+    if (hint_ns == 0u) {
+      asm volatile(
+          "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+          : "=r"(ok)
+          : "r"(smem_u32(m)), "r"(parity)
+          : "memory");
+    } else {
+      asm volatile(
+          "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+          : "=r"(ok)
+          : "r"(smem_u32(m)), "r"(parity)
+          : "memory");
+      if (!ok) __nanosleep(hint_ns);
+    }
     if (ok) return true;
   }
   return false;
 }
+
+// The ring's wait limits, from the plan.
+struct WaitCfg {
+  uint32_t spin_limit, spin_hint_ns;
+};
 
 __device__ __forceinline__ void cp_async4(void* dst, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
@@ -182,6 +201,40 @@ __device__ __forceinline__ int elem_index(int ch, int v, int jj) {
 
 // Everything the out-of-line paths need to recompute a stage element's
 // processed value, by value (nothing of the hot loop's state is addressed).
+// A row's temperature step: x / T, one IEEE fp32 division (rounded to
+// nearest) for stochastic rows; greedy rows keep x.
+struct Temp {
+  float T;
+  bool stoch;
+};
+__device__ __forceinline__ Temp temp_of(const RowCtx& rc) { return Temp{rc.T, rc.stoch}; }
+__device__ __forceinline__ float temper(float x, Temp tp) { return tp.stoch ? __fdiv_rn(x, tp.T) : x; }
+
+// The largest raw value x0 (or less) whose processed value lies below the
+// packed cut: every x <= x0 has fl(x / T) < cut's value, since rounding x / T
+// (T > 0) is monotone in x.  NaN (no raw value is skipped) when the cut
+// admits everything or the search does not settle.
+__device__ __noinline__ float raw_threshold(unsigned long long cut, Temp tp) {
+  const uint32_t ck = pk_key(cut);
+  if (ck <= kKeyNegInf) return __int_as_float(0x7FC00000);
+  const float cf = key2f(ck);  // processed values below cf key below ck
+  if (!tp.stoch) return nextafterf(cf, -INFINITY);
+  float x = __fmul_rn(cf, tp.T);
+  for (int i = 0; i < 8; ++i) {
+    if (__fdiv_rn(x, tp.T) < cf) return x;
+    x = nextafterf(x, -INFINITY);
+  }
+  return __int_as_float(0x7FC00000);
+}
+
+// x / T for the normaliser partials only, which tolerate an ulp: the
+// quotient q = RN(x * r) with r = RN(1 / T), corrected once by the residual
+// x - q * T (Markstein's division step, IBM J. Res. Dev. 34(1), 1990).
+__device__ __forceinline__ float quot_lse(float x, float T, float r) {
+  const float q = __fmul_rn(x, r);
+  return __fmaf_rn(__fmaf_rn(-q, T, x), r, q);
+}
+
 struct StageCtx {
   const unsigned char* ring;
   const uint32_t* msl;           // the stage's mask words (shared or global), or null
@@ -228,7 +281,7 @@ __device__ __forceinline__ float value_with(const StageCtx& s, int li, uint32_t 
   float v = raw_at<BF16>(s.ring, li);
   if (s.msl && ((s.msl[li >> 5] >> (li & 31)) & 1u) == 0u) v = -INFINITY;
   if (info) v = apply_penalty_bias(v, info & 0x7FFFFFFFu, (info >> 31) != 0u, s.t0 + li, s.rc, s.bl);
-  return __fmul_rn(v, s.rc.rT);
+  return apply_temperature(v, s.rc);
 }
 
 // Exact top-`need` of the stage, appended to cand[cbase + *acnt]: MSB-first
@@ -378,12 +431,13 @@ __device__ __noinline__ Raised raise_cut(unsigned long long* cand, unsigned long
   return Raised{nc, m};
 }
 
-// Load chunk ch of the stage and apply mask and temperature; returns the
-// NaN-propagating maximum.  MASK: msl holds the stage's mask words (shared or
+// Load chunk ch of the stage with the mask applied (masked elements -inf) but
+// not the temperature: raw values, which the cut tests compare with the cut's
+// raw threshold; returns their NaN-propagating maximum.  MASK: msl holds the stage's mask words (shared or
 // global memory).  FULL: the stage has B_N tokens (otherwise elements past
 // the last token read as -inf and are never appended).
 template <bool BF16, bool MASK, bool FULL>
-__device__ __forceinline__ float load_chunk(const unsigned char* ring, const uint32_t* msl, float rT, int ch, int nt,
+__device__ __forceinline__ float load_chunk(const unsigned char* ring, const uint32_t* msl, int ch, int nt,
                                             float (&x)[kPT]) {
   constexpr int VEC = BF16 ? 8 : 4;
   constexpr int NV = kPT / VEC;
@@ -400,7 +454,6 @@ __device__ __forceinline__ float load_chunk(const unsigned char* ring, const uin
       if constexpr (MASK) {
         if (((bits >> jj) & 1u) == 0u) val = -INFINITY;
       }
-      val = __fmul_rn(val, rT);
       if (!FULL && e0 + jj >= nt) val = -INFINITY;
       x[v * VEC + jj] = val;
     }
@@ -419,18 +472,18 @@ __device__ __forceinline__ float load_chunk(const unsigned char* ring, const uin
 
 template <bool BF16>
 __device__ __forceinline__ float load_chunk_sel(bool mask, bool full, const unsigned char* ring, const uint32_t* msl,
-                                                float rT, int ch, int nt, float (&x)[kPT]) {
+                                                int ch, int nt, float (&x)[kPT]) {
   if (mask)
-    return full ? load_chunk<BF16, true, true>(ring, msl, rT, ch, nt, x)
-                : load_chunk<BF16, true, false>(ring, msl, rT, ch, nt, x);
-  return full ? load_chunk<BF16, false, true>(ring, msl, rT, ch, nt, x)
-              : load_chunk<BF16, false, false>(ring, msl, rT, ch, nt, x);
+    return full ? load_chunk<BF16, true, true>(ring, msl, ch, nt, x)
+                : load_chunk<BF16, true, false>(ring, msl, ch, nt, x);
+  return full ? load_chunk<BF16, false, true>(ring, msl, ch, nt, x)
+              : load_chunk<BF16, false, false>(ring, msl, ch, nt, x);
 }
 
-// Vector v of chunk ch of a full stage with mask and temperature applied
-// (the same fp32 steps as load_chunk, so the same bits).
+// Vector v of chunk ch of a full stage with the mask applied (raw values,
+// as load_chunk gives them).
 template <bool BF16, bool MASK>
-__device__ __forceinline__ void load_vec(const unsigned char* ring, const uint32_t* msl, float rT, int ch, int v,
+__device__ __forceinline__ void load_vec(const unsigned char* ring, const uint32_t* msl, int ch, int v,
                                          float* y) {
   constexpr int VEC = BF16 ? 8 : 4;
   const int e0 = elem_index<VEC>(ch, v, 0);
@@ -443,7 +496,7 @@ __device__ __forceinline__ void load_vec(const unsigned char* ring, const uint32
     if constexpr (MASK) {
       if (((bits >> jj) & 1u) == 0u) val = -INFINITY;
     }
-    y[jj] = __fmul_rn(val, rT);
+    y[jj] = val;
   }
 }
 
@@ -454,10 +507,9 @@ __device__ __forceinline__ uint32_t bf16x2_max_nan(uint32_t a, uint32_t b) {
 }
 
 // NaN-propagating maxima of the RAW values of chunk ch (no mask, no
-// temperature), per vector in vm and overall.  For rT > 0, rounding x * rT is
-// monotone in x, so a chunk whose raw maximum m has fl(m * rT) below the cut
-// holds no processed value at or above it (masked values are -inf); with
-// rT = +inf, m >= 0 gives +inf or NaN and the chunk is examined.
+// temperature), per vector in vm and overall.  A chunk whose raw maximum m
+// is at most the raw threshold of the cut (raw_threshold) holds no processed
+// value at or above the cut (masked values are -inf).
 template <bool BF16>
 __device__ __forceinline__ float raw_chunk_max(const unsigned char* ring, int ch, float (&vm)[kPT / (BF16 ? 8 : 4)]) {
   constexpr int VEC = BF16 ? 8 : 4;
@@ -487,10 +539,10 @@ __device__ __forceinline__ float raw_chunk_max(const unsigned char* ring, int ch
 // The value the stream computes for stage element li (mask and temperature:
 // the same fp32 steps as load_chunk, so the same bits).
 template <bool BF16>
-__device__ __forceinline__ float stream_value(const unsigned char* ring, const uint32_t* msl, float rT, int li) {
+__device__ __forceinline__ float stream_value(const unsigned char* ring, const uint32_t* msl, Temp tp, int li) {
   float v = raw_at<BF16>(ring, li);
   if (msl && ((msl[li >> 5] >> (li & 31)) & 1u) == 0u) v = -INFINITY;
-  return __fmul_rn(v, rT);
+  return temper(v, tp);
 }
 
 // 2^x by the hardware approximation (PTX ex2.approx, relative error about
@@ -509,7 +561,7 @@ __device__ __forceinline__ float ex2_approx(float x) {
 // i % 4.  Tokens the count table lists (aux != 0) join with their exact values
 // elsewhere; NaN and -inf values take no part.
 template <bool BF16>
-__device__ __noinline__ void chunk_gmax(const unsigned char* ring, const uint32_t* msl, float rT, int ch, int nt,
+__device__ __noinline__ void chunk_gmax(const unsigned char* ring, const uint32_t* msl, Temp tp, int ch, int nt,
                                         bool full, const uint16_t* aux, int t0, uint32_t gpos, uint32_t row,
                                         const uint64_t* seeds, unsigned long long* gmax) {
   constexpr int VEC = BF16 ? 8 : 4;
@@ -530,7 +582,7 @@ __device__ __noinline__ void chunk_gmax(const unsigned char* ring, const uint32_
         const int li = b0 + k;
         if (!full && li >= nt) break;
         if (aux && aux[li] != 0u) continue;
-        const float xv = stream_value<BF16>(ring, msl, rT, li);
+        const float xv = stream_value<BF16>(ring, msl, tp, li);
         if (xv > -INFINITY) {
           const float sc = __fadd_rn(xv, gumbel_of(word_to_uniform(wd[k])));
           const unsigned long long pk = pack(f2key(sc), (uint32_t)(t0 + li));
@@ -654,6 +706,9 @@ __global__ void __launch_bounds__(kNT, 2) stage1_kernel(const Params P) {
   cp_async_wait_all();
   __syncthreads();
 
+  WaitCfg R;
+  R.spin_limit = P.spin_limit;
+  R.spin_hint_ns = P.spin_hint_ns;
   long long g = g0;
   int kst = 0;           // stages consumed by this CTA
   int slot = 0;          // kst % NS
@@ -669,6 +724,7 @@ __global__ void __launch_bounds__(kNT, 2) stage1_kernel(const Params P) {
     const long long ge = min(g1, gs + Z);
     const size_t lslot = slot_of(pos);
     const RowCtx rc = make_row(cb.rp, P.hist_stride, P.bias_stride);
+    const Temp tp = temp_of(rc);
     // the next segment's bookkeeping (the next position; rows own consecutive positions)
     if (warp == 0 && ge < g1) {
       const int pn = pos + 1;
@@ -769,6 +825,11 @@ __global__ void __launch_bounds__(kNT, 2) stage1_kernel(const Params P) {
     const int nf = hashed ? sm.nf : 0;
 
     unsigned long long cutp = 0ull;  // packed cut (0: everything)
+    // the raw threshold of the cut x0cut: raw values <= x0 lie below it (NaN:
+    // none is known to; the cut 0 admits everything)
+    float x0 = __int_as_float(0x7FC00000);
+    unsigned long long x0cut = 0ull;
+    const float rTl = tp.stoch ? __frcp_rn(tp.T) : 1.0f;  // for the normaliser's quotients
     int n = nf;                      // buffer entries (uniform; read between barriers)
     float lM = -INFINITY, lS = 0.0f; // this thread's running (max, sum exp) for the normaliser
     bool first = true;
@@ -784,7 +845,7 @@ __global__ void __launch_bounds__(kNT, 2) stage1_kernel(const Params P) {
       // the next stage's counter was last read after the barrier two stages back
       if (tid == 0) sm.cnt[c3 == 2 ? 0 : c3 + 1] = 0;
       // a copy that never lands is noticed by all threads after the stage barrier
-      if (!mbar_wait(&sm.mbar[slot], phase)) sm.dead = 1;
+      if (!mbar_wait(&sm.mbar[slot], phase, R.spin_limit, R.spin_hint_ns)) sm.dead = 1;
 
       if (rc.valid) {
         // per-stage count table (long histories, normaliser positions)
@@ -842,8 +903,10 @@ __global__ void __launch_bounds__(kNT, 2) stage1_kernel(const Params P) {
         const bool merged = first && nch == 1;
         const bool lazy = !first && full && !lse_on && !gmax_on;
         for (int pass = (first && !merged) ? 0 : 1; pass < 2; ++pass) {
-          uint32_t ck = pk_key(cutp);
-          float cut_f = ck <= kKeyNegInf ? -INFINITY : key2f(ck);
+          if (pass == 1 && cutp != x0cut) {
+            x0 = raw_threshold(cutp, tp);
+            x0cut = cutp;
+          }
           float mt = -INFINITY;
           for (int ch = 0; ch < nch; ++ch) {
             if (lazy) {
@@ -851,26 +914,27 @@ __global__ void __launch_bounds__(kNT, 2) stage1_kernel(const Params P) {
               // and only the vectors that may hold a hit are processed
               float vm[NV];
               const float m = raw_chunk_max<BF16>(ring, ch, vm);
-              if (!(__fmul_rn(m, rc.rT) < cut_f)) {
+              if (!(m <= x0)) {
                 uint32_t vb = 0u;
 #pragma unroll
-                for (int v = 0; v < NV; ++v) vb |= (__fmul_rn(vm[v], rc.rT) < cut_f ? 0u : 1u) << v;
+                for (int v = 0; v < NV; ++v) vb |= (vm[v] <= x0 ? 0u : 1u) << v;
                 while (vb) {
                   const int v = __ffs((int)vb) - 1;
                   vb &= vb - 1u;
                   float y[VEC];
-                  if (mask_on) load_vec<BF16, true>(ring, msl, rc.rT, ch, v, y);
-                  else load_vec<BF16, false>(ring, msl, rc.rT, ch, v, y);
+                  if (mask_on) load_vec<BF16, true>(ring, msl, ch, v, y);
+                  else load_vec<BF16, false>(ring, msl, ch, v, y);
                   uint32_t bits = 0u;
 #pragma unroll
-                  for (int jj = 0; jj < VEC; ++jj) bits |= (y[jj] < cut_f ? 0u : 1u) << jj;
+                  for (int jj = 0; jj < VEC; ++jj) bits |= (y[jj] <= x0 ? 0u : 1u) << jj;
                   const int e0 = elem_index<VEC>(ch, v, 0);
                   while (bits) {
                     const int jj = __ffs((int)bits) - 1;
                     bits &= bits - 1u;
-                    float xv = y[0];
+                    float xr = y[0];
 #pragma unroll
-                    for (int k = 1; k < VEC; ++k) xv = jj == k ? y[k] : xv;
+                    for (int k = 1; k < VEC; ++k) xr = jj == k ? y[k] : xr;
+                    const float xv = temper(xr, tp);
                     const int li = e0 + jj;
                     const bool isn = xv != xv;
                     nan_seen |= isn;
@@ -885,7 +949,7 @@ __global__ void __launch_bounds__(kNT, 2) stage1_kernel(const Params P) {
               continue;
             }
             float x[kPT];
-            const float m = load_chunk_sel<BF16>(mask_on, full, ring, msl, rc.rT, ch, nt, x);
+            const float m = load_chunk_sel<BF16>(mask_on, full, ring, msl, ch, nt, x);
             if (pass == 0) {
 #pragma unroll
               for (int e = 0; e < kPT; ++e) mt = fmaxf(mt, x[e]);
@@ -898,21 +962,21 @@ __global__ void __launch_bounds__(kNT, 2) stage1_kernel(const Params P) {
 #pragma unroll
                 for (int e = 0; e < kPT; ++e) mc = fmaxf(mc, x[e]);
               }
-              cutp = certify(mc);
-              ck = pk_key(cutp);
-              cut_f = ck <= kKeyNegInf ? -INFINITY : key2f(ck);
+              cutp = certify(temper(mc, tp));  // the largest processed value (temper is monotone)
+              x0 = raw_threshold(cutp, tp);
+              x0cut = cutp;
             }
-            if (!(m < cut_f)) {
+            if (!(m <= x0)) {
               // elements at or above the cut (or NaN): re-derived from the slot
               uint32_t bits = 0u;
 #pragma unroll
-              for (int e = 0; e < kPT; ++e) bits |= (x[e] < cut_f ? 0u : 1u) << e;
+              for (int e = 0; e < kPT; ++e) bits |= (x[e] <= x0 ? 0u : 1u) << e;
               while (bits) {
                 const int e = __ffs((int)bits) - 1;
                 bits &= bits - 1u;
                 const int li = ((ch * NV + e / VEC) * kNT + tid) * VEC + e % VEC;
                 if (!full && li >= nt) continue;
-                const float xv = stream_value<BF16>(ring, msl, rc.rT, li);
+                const float xv = stream_value<BF16>(ring, msl, tp, li);
                 const bool isn = xv != xv;
                 nan_seen |= isn;
                 const unsigned long long pk = pack(isn ? kKeyNegInf : f2key(xv), (uint32_t)(t0 + li));
@@ -923,26 +987,26 @@ __global__ void __launch_bounds__(kNT, 2) stage1_kernel(const Params P) {
               }
             }
             if (lse_on) {
-              // the chunk's maximum without NaN: load_chunk's (NaN-propagating)
-              // maximum unless a NaN or a count-table row needs it recomputed
-              float mc = m;
-              if (staged || mc != mc) {
-                if (staged) {
+              // the processed values (x / T, to an ulp) and their maximum
+              // without NaN; listed tokens (count-table rows) are added with
+              // their exact values elsewhere
 #pragma unroll
-                  for (int e = 0; e < kPT; ++e) {
-                    const int li = elem_index<VEC>(ch, e / VEC, e % VEC);
-                    if ((full || li < nt) && aux[li] != 0u) x[e] = -INFINITY;  // added with its exact value
-                  }
+              for (int e = 0; e < kPT; ++e) x[e] = quot_lse(x[e], tp.T, rTl);
+              if (staged) {
+#pragma unroll
+                for (int e = 0; e < kPT; ++e) {
+                  const int li = elem_index<VEC>(ch, e / VEC, e % VEC);
+                  if ((full || li < nt) && aux[li] != 0u) x[e] = -INFINITY;
                 }
-                float t[kPT / 2];
-#pragma unroll
-                for (int e = 0; e < kPT / 2; ++e) t[e] = fmaxf(x[2 * e], x[2 * e + 1]);
-#pragma unroll
-                for (int w = kPT / 4; w >= 1; w >>= 1)
-#pragma unroll
-                  for (int e = 0; e < w; ++e) t[e] = fmaxf(t[e], t[e + w]);
-                mc = t[0];
               }
+              float t[kPT / 2];
+#pragma unroll
+              for (int e = 0; e < kPT / 2; ++e) t[e] = fmaxf(x[2 * e], x[2 * e + 1]);
+#pragma unroll
+              for (int w = kPT / 4; w >= 1; w >>= 1)
+#pragma unroll
+                for (int e = 0; e < w; ++e) t[e] = fmaxf(t[e], t[e + w]);
+              const float mc = t[0];
               if (mc > -INFINITY) {
                 const float Mn = fmaxf(lM, mc);
                 const float off = Mn * kLog2e;
@@ -956,7 +1020,7 @@ __global__ void __launch_bounds__(kNT, 2) stage1_kernel(const Params P) {
               }
             }
           }
-          if (pass == 0) cutp = certify(mt);
+          if (pass == 0) cutp = certify(temper(mt, tp));  // the largest processed value
         }
         // the listed tokens' exact values (hash mode), from the loads issued at set-up
         if (first && hashed) {
@@ -970,7 +1034,7 @@ __global__ void __launch_bounds__(kNT, 2) stage1_kernel(const Params P) {
               float v = fl_raw[k];
               if (((fl_mw[k] >> (tok & 31)) & 1u) == 0u) v = -INFINITY;
               v = apply_penalty_bias(v, info & 0x7FFFFFFFu, (info >> 31) != 0u, tok, rc, bl);
-              v = __fmul_rn(v, rc.rT);
+              v = apply_temperature(v, rc);
               nan_seen |= v != v;
               cand[i] = pack(v != v ? kKeyNegInf : f2key(v), (uint32_t)tok);
             }
@@ -1055,7 +1119,7 @@ __global__ void __launch_bounds__(kNT, 2) stage1_kernel(const Params P) {
       // refilled (and from the stage's count table, still in place)
       if (gmax_on) {
         for (int ch = 0; ch < nch; ++ch)
-          chunk_gmax<BF16>(ring, msl, rc.rT, ch, nt, full, staged ? aux : nullptr, t0, rc.position + (uint32_t)j,
+          chunk_gmax<BF16>(ring, msl, tp, ch, nt, full, staged ? aux : nullptr, t0, rc.position + (uint32_t)j,
                            (uint32_t)r, P.seeds, &sm.gmax);
         __syncthreads();  // every read of the slot is done before its refill
       }
@@ -1071,6 +1135,7 @@ __global__ void __launch_bounds__(kNT, 2) stage1_kernel(const Params P) {
         cutp = rz.cut;
         n_end = rz.n;
         if (n_end > kCompactAt) {
+          if (tid == 0) atomicAdd(P.ws.diag + 4, 1u);
           cutp = compact(cand, tmp, outb, n_end, sm);
           n_end = kK;
         }
@@ -1121,20 +1186,24 @@ __global__ void __launch_bounds__(kNT, 2) stage1_kernel(const Params P) {
 
   if (dead) {
     // A bulk copy did not complete within the wait limit: count it, leave
-    // empty lists for this and the remaining positions of the range, and let
-    // the copies still in flight land (bounded waits) before the CTA exits.
+    // empty lists with SS_ST_COPY_TIMEOUT for this and the remaining
+    // positions of the range, and let the copies still in flight (the stages
+    // kst .. kst + NS - 1 of the range) land, with the long drain limit,
+    // before the CTA exits.
     if (tid == 0) atomicAdd(P.ws.diag + 3, 1u);
     const int p_first = (int)(g / Z), p_last = (int)((g1 - 1) / Z);
     for (int p = p_first; p <= p_last; ++p) {
       const size_t ls = slot_of(p);
       for (int q = tid; q < kK; q += kNT) P.ws.staging[ls * kK + q] = 0ull;
       if (tid == 0) {
-        P.ws.tile_status[ls] = 0u;
+        P.ws.tile_status[ls] = (uint32_t)SS_ST_COPY_TIMEOUT;
         P.ws.tile_lse[ls] = make_float2(-INFINITY, 0.0f);
+        P.ws.tile_gmax[ls] = 0ull;
       }
     }
     if (tid == 0)
-      for (int s = 0; s < NS && g + s < g1; ++s) mbar_wait(&sm.mbar[(kst + s) % NS], (uint32_t)(((kst + s) / NS) & 1));
+      for (int s = 0; s < NS && g + s < g1; ++s)
+        mbar_wait(&sm.mbar[(kst + s) % NS], (uint32_t)(((kst + s) / NS) & 1), kDrainSpin, 0u);
     cp_async_wait_all();
     __syncthreads();
   }

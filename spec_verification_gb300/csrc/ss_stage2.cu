@@ -84,7 +84,7 @@ __device__ float prelude_single_warp(const Params& P, const RowCtx& rc, int pos,
   }
   const ss_bias_entry* brow = (rc.flags & SS_BIAS) && P.bias ? P.bias + (size_t)r * P.bias_stride : nullptr;
   x = apply_penalty_bias(x, (uint32_t)cnt, brow != nullptr, tok, rc, brow);
-  if (rc.stoch) x = __fmul_rn(x, rc.rT);
+  x = apply_temperature(x, rc);
   if (x != x) x = -INFINITY;
   return x;
 }

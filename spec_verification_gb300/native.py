@@ -17,8 +17,12 @@ SS_F32, SS_BF16 = 0, 1
 STATUS = {0: "SS_OK", -1: "SS_ERR_ARG", -2: "SS_ERR_ALIGN", -3: "SS_ERR_UNSUPPORTED",
           -4: "SS_ERR_WORKSPACE", -5: "SS_ERR_CUDA"}
 K = 128
+# row_status bit of a row with invalid parameters (SS_ST_BAD_PARAM)
+ST_BAD_PARAM = 1 << 4
 # row_status bit of a verification row past the plan's max_positions (SS_ST_CAPACITY)
 ST_CAPACITY = 1 << 9
+# row_status bit of a row whose stage-1 copy did not land within the wait limit
+ST_COPY_TIMEOUT = 1 << 10
 
 # numpy layouts of the device-side structs (all 4-byte fields, no padding)
 ROW_DTYPE = np.dtype([("flags", "<u4"), ("temperature", "<f4"), ("top_p", "<f4"), ("min_p", "<f4"),
@@ -50,7 +54,7 @@ class Out(C.Structure):
 
 EXPORTS = ["ss_plan_create", "ss_plan_destroy", "ss_workspace_bytes", "ss_plan_tile",
            "ss_plan_num_tiles", "ss_plan_stage1_ctas", "ss_sample", "ss_verify", "ss_status_str", "ss_last_error",
-           "ss_workspace_diag_offset", "ss_sample_noalloc", "ss_plan_enable_exact"]
+           "ss_workspace_diag_offset", "ss_sample_noalloc", "ss_plan_enable_exact", "ss_plan_set_wait_limit"]
 
 _lib = None
 
@@ -80,6 +84,8 @@ def library() -> C.CDLL:
     L.ss_plan_stage1_ctas.restype = C.c_int32
     L.ss_plan_enable_exact.argtypes = [C.c_void_p, C.c_int]
     L.ss_plan_enable_exact.restype = C.c_int
+    L.ss_plan_set_wait_limit.argtypes = [C.c_void_p, C.c_uint32, C.c_uint32]
+    L.ss_plan_set_wait_limit.restype = C.c_int
     L.ss_sample.argtypes = [C.c_void_p, C.POINTER(Batch), C.c_void_p, C.c_void_p, C.c_void_p,
                             C.c_void_p, C.POINTER(Out)]
     L.ss_sample.restype = C.c_int
@@ -122,6 +128,11 @@ class Plan:
     def enable_exact(self, on: bool = True):
         """Run the exact-sampling variant of stage 1 (rows flagged SS_EXACT)."""
         _check(library().ss_plan_enable_exact(self._p, 1 if on else 0))
+
+    def set_wait_limit(self, polls: int, suspend_ns: int = 0):
+        """Polls of a stage-1 copy wait before the copy counts as lost (0:
+        default) and the suspend-time hint of each poll (0: the hardware's)."""
+        _check(library().ss_plan_set_wait_limit(self._p, polls, suspend_ns))
 
     @property
     def handle(self):
