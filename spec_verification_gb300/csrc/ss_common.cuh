@@ -456,9 +456,11 @@ __device__ void block_select(unsigned long long* cand, unsigned long long* tmp, 
     S.tcnt[1] = 0;
   }
   __syncthreads();
+#pragma unroll 1
   for (int iter = 0; iter < 16; ++iter) {
     if (need <= 0) break;
     if (n <= need) {
+#pragma unroll 1
       for (int i = tid; i < n; i += NT) emit(cand[i]);
       break;
     }
@@ -478,6 +480,7 @@ __device__ void block_select(unsigned long long* cand, unsigned long long* tmp, 
     const unsigned long long span = hi - lo;
     int shift = 0;
     if (span != 0ull) shift = max(0, 64 - __clzll((long long)span) - 8);
+#pragma unroll 1
     for (int i = tid; i < n; i += NT) atomicAdd(&S.hist[bin_of(cand[i], lo, shift)], 1u);
     __syncthreads();
     boundary_bin(S, need);
@@ -485,6 +488,7 @@ __device__ void block_select(unsigned long long* cand, unsigned long long* tmp, 
     const int ab = S.above;
     const int nb = S.nb;
     int* tc = &S.tcnt[iter & 1];
+#pragma unroll 1
     for (int i = tid; i < n; i += NT) {
       const unsigned long long c = cand[i];
       const uint32_t b = bin_of(c, lo, shift);

@@ -54,6 +54,9 @@ namespace ss {
 namespace {
 
 constexpr uint32_t kDrainSpin = 1u << 22;  // polls of the final drain of copies in flight
+// Loops of the cold paths (selection, hashing, raises) are kept rolled
+// (#pragma unroll 1): each kernel instance is then about 207 KB of code
+// instead of 275 KB, and measured 3-5 % faster.
 constexpr int kMaxSlots = 4;         // ring slots at most
 constexpr int kCap = 1024;           // candidate buffer entries
 constexpr int kRaiseAt = 384;        // buffer fill that triggers a cut raise
@@ -220,6 +223,7 @@ __device__ __noinline__ float raw_threshold(unsigned long long cut, Temp tp) {
   const float cf = key2f(ck);  // processed values below cf key below ck
   if (!tp.stoch) return nextafterf(cf, -INFINITY);
   float x = __fmul_rn(cf, tp.T);
+#pragma unroll 1
   for (int i = 0; i < 8; ++i) {
     if (__fdiv_rn(x, tp.T) < cf) return x;
     x = nextafterf(x, -INFINITY);
@@ -252,6 +256,7 @@ __device__ __forceinline__ uint32_t hash_of(int tok) { return ((uint32_t)tok * 0
 // Slot of token tok in the segment's hash table, or -1.
 __device__ __forceinline__ int hash_find(const int* hkey, int tok) {
   uint32_t h = hash_of(tok);
+#pragma unroll 1
   for (int probe = 0; probe < kHash; ++probe) {
     const int k = hkey[h];
     if (k == tok) return (int)h;
@@ -311,6 +316,7 @@ __device__ __noinline__ void stage_exact(const StageCtx& s, S1Smem& sm, int* acn
   if (nan_seen) sm.nan_flag = 1;
   uint32_t prefix = 0u, pmask = 0u;
   int rem = need;
+#pragma unroll 1
   for (int d = 0; d < 4; ++d) {
     const int shift = 24 - 8 * d;
     sm.sel.hist[tid & 255] = 0u;
@@ -364,6 +370,7 @@ template <class Emit>
 __device__ __forceinline__ void select_top(unsigned long long* cand, unsigned long long* tmp, int n, int need,
                                            S1Smem& sm, Emit emit) {
   unsigned long long mn = ~0ull, mx = 0ull;
+#pragma unroll 1
   for (int i = threadIdx.x; i < n; i += kNT) {
     const unsigned long long c = cand[i];
     mn = c < mn ? c : mn;
@@ -403,10 +410,12 @@ __device__ __noinline__ Raised raise_cut(unsigned long long* cand, unsigned long
   if (tid < 256) sm.sel.hist[tid] = 0u;
   if (tid == 0) sm.out_cnt = 0;
   unsigned long long mx = 0ull;
+#pragma unroll 1
   for (int i = tid; i < n; i += kNT) mx = cand[i] > mx ? cand[i] : mx;
   mx = block_max_u64(mx, sm.slots);
   const int shift = mx > cut ? max(0, 64 - __clzll((long long)(mx - cut)) - 8) : 0;
   if (mx > cut)
+#pragma unroll 1
     for (int i = tid; i < n; i += kNT) atomicAdd(&sm.sel.hist[bin_of(cand[i], cut, shift)], 1u);
   __syncthreads();
   boundary_bin(sm.sel, kK);
@@ -416,6 +425,7 @@ __device__ __noinline__ Raised raise_cut(unsigned long long* cand, unsigned long
     return Raised{cut, n};
   }
   const unsigned long long nc = cut + ((unsigned long long)bstar << shift);
+#pragma unroll 1
   for (int i = tid; i < n; i += kNT) {
     const unsigned long long c = cand[i];
     if (c >= nc) tmp[atomicAdd(&sm.out_cnt, 1)] = c;
@@ -426,6 +436,7 @@ __device__ __noinline__ Raised raise_cut(unsigned long long* cand, unsigned long
   // selection (compact, the segment end), and a warp that saw the reset count
   // would take other branches (and barriers) than the rest of the block
   const int m = sm.out_cnt;
+#pragma unroll 1
   for (int i = tid; i < m; i += kNT) cand[i] = tmp[i];
   __syncthreads();
   return Raised{nc, m};
@@ -638,10 +649,17 @@ __global__ void __launch_bounds__(kNT, 2) stage1_kernel(const Params P) {
   const bool mask_tma = P.mask_tma != 0 && P.bitmask != nullptr;
   const int nch = BN / kChunk;
 
-  // thread 0: bulk copies of stage g (logits, then the mask words) into a slot
-  auto issue = [&](long long g, int slot) {
-    const int pos = (int)(g / Z);
-    const int t0 = (int)(g - (long long)pos * Z) * BN;
+  // thread 0: bulk copies of the next stage of the range (logits, then the
+  // mask words) into a slot.  Stages are issued in order, so the position
+  // and tile of the next one advance by one tile per call.
+  int iss_pos = (int)(g0 / Z), iss_tile = (int)(g0 - (long long)iss_pos * Z);
+  auto issue = [&](int slot) {
+    const int pos = iss_pos;
+    const int t0 = iss_tile * BN;
+    if (++iss_tile == Z) {
+      iss_tile = 0;
+      ++iss_pos;
+    }
     const int nt = min(BN, V - t0);
     const uint32_t bytes = (uint32_t)((nt * ESZ + 15) & ~15);
     const uint32_t mbytes = mask_tma ? (uint32_t)((((nt + 31) >> 5) * 4 + 15) & ~15) : 0u;
@@ -691,7 +709,7 @@ __global__ void __launch_bounds__(kNT, 2) stage1_kernel(const Params P) {
     sm.dead = 0;
     for (int s = 0; s < NS; ++s) mbar_init(&sm.mbar[s]);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    for (int s = 0; s < NS && g0 + s < g1; ++s) issue(g0 + s, s);
+    for (int s = 0; s < NS && g0 + s < g1; ++s) issue(s);
   }
   if (warp == 0) {
     const int pos = (int)(g0 / Z);
@@ -783,6 +801,7 @@ __global__ void __launch_bounds__(kNT, 2) stage1_kernel(const Params P) {
       auto insert = [&](int tok, uint32_t add, uint32_t orv) {
         if (tok < seg_lo || tok >= seg_hi) return;  // also drops padding (< 0) and ids >= V
         uint32_t h = hash_of(tok);
+#pragma unroll 1
         for (int probe = 0; probe < kHash; ++probe) {
           const int old = atomicCAS(&hkey[h], -1, tok);
           if (old == -1 || old == tok) {
@@ -1126,7 +1145,7 @@ __global__ void __launch_bounds__(kNT, 2) stage1_kernel(const Params P) {
       // refill this slot with the stage NS ahead (every read of it is done)
       if (tid == 0 && g + NS < g1) {
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        issue(g + NS, slot);
+        issue(slot);
       }
       // ---- keep room in the buffer: one histogram pass raises the cut; the
       // exact top-128 only if that left too many (a crowd of equal values)
