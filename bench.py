@@ -367,21 +367,16 @@ def graph_copies(R: int, G: int) -> list:
     return [[(j * G + i) % R for i in range(G)] for j in range(NG)]
 
 
-def run_ours(args, w, desc):
+def time_device(args, w, dev, world, K, Wm, tile=0):
+    """Graph-replayed timing of K calls of workload w with inputs resident in
+    HBM (after Wm warm-up calls): returns the run, the slowest rank's time of
+    the K calls (ms), the per-kernel durations of the last G calls (us) and
+    the clock record of the timed region."""
     import torch
     import torch.distributed as dist
-    from spec_verification_gb300 import build
     from spec_verification_gb300.runner import DeviceRun
 
-    world, rank, local = dist_setup()
-    if world > 1:
-        dist.init_process_group("nccl")
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    build.build()
-    run = DeviceRun(w, device=str(dev), candidates=False, tile=args.tile)
-    verify = w.is_verify
-    K, Wm = args.steps, args.warmup
+    run = DeviceRun(w, device=str(dev), candidates=False, tile=tile)
     G = max(d for d in range(1, min(10, K) + 1) if K % d == 0)
     # resident copies of the streamed inputs, walked in turn so that nothing
     # is served from L2 (together at least twice its size)
@@ -427,7 +422,7 @@ def run_ours(args, w, desc):
         graph_ev.replay()
     stream.synchronize()
 
-    clocks = Clocks(local)
+    clocks = Clocks(dev.index or 0)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize(dev)
@@ -446,12 +441,98 @@ def run_ours(args, w, desc):
     if world > 1:
         dist.barrier()
     ms = t_start.elapsed_time(t_end)
-    st1 = [event_ms(ev[i][0], ev[i][1]) for i in range(G)]
-    st2 = [event_ms(ev[i][1], ev[i][2]) for i in range(G)]
-    st3 = [event_ms(ev[i][2], ev[i][3]) for i in range(G)]
+    stages = {"stage1": 1e3 * statistics.mean(event_ms(ev[i][0], ev[i][1]) for i in range(G)),
+              "stage2": 1e3 * statistics.mean(event_ms(ev[i][1], ev[i][2]) for i in range(G)),
+              "residual": 1e3 * statistics.mean(event_ms(ev[i][2], ev[i][3]) for i in range(G)) if w.is_verify else 0.0}
     ms_max = max_over_ranks(ms, world, dev)
+    info = {"R": R, "call_bytes": call_bytes, "l2": l2, "G": G, "NG": NG}
+    del graphs, graph_ev, lg, qq
+    return run, ms_max, stages, ck, info
 
-    # end to end: inputs from pinned host memory, tokens back, every step
+
+def roofline_of(w, run, stages, ms_max, K, peak, peak_kind, traffic=None) -> tuple:
+    """The stage-1 roofline and the whole call's counted-byte rate."""
+    alg1 = stage1_alg_bytes(w, run.plan.tile, run.plan.stage1_ctas)
+    achieved = alg1 / (stages["stage1"] / 1e6) / 1e9
+    roof = {"bound": "hbm", "kernel": "stage1", "achieved": achieved, "peak": peak, "unit": "GB/s",
+            "frac": achieved / peak, "peak_kind": peak_kind, "traffic": traffic, "alg_bytes_per_launch": alg1}
+    counted = w.counted_bytes(8192)  # the metric's definition: staging of 8192-token tiles
+    s_call = ms_max / K / 1e3
+    hbm = {"counted_bytes_per_call": counted, "counted_gbs": counted / s_call / 1e9,
+           "counted_frac": counted / s_call / 1e9 / peak,
+           "read_bytes_per_call": alg1 + stage2_read_bytes(w, run),
+           "read_frac": (alg1 + stage2_read_bytes(w, run)) / s_call / 1e9 / peak,
+           "note": ("counted = logits + bitmask + draft probabilities + staging write and read of 8192-token "
+                    "tiles per call, the metric's definition; the kernels read only q(d) of each draft and the q "
+                    "rows of rejected untruncated positions, so counted_frac overstates the bytes moved when q "
+                    "is large.  read = stage-1 algorithmic bytes + the staging lists stage 2 reads: the bytes "
+                    "the call must move")}
+    return roof, hbm
+
+
+def stage2_read_bytes(w, run) -> int:
+    """Bytes stage 2 reads: each segment's 128 packed candidates and its metadata."""
+    z = run.plan.num_tiles
+    return num_segments(w.n_positions, z, run.plan.stage1_ctas) * (128 * 8 + 12)
+
+
+def h2d_copy_rate(dev, nbytes: int, streams: int) -> float:
+    """GB/s of a plain pinned host -> device copy of nbytes, split over
+    `streams` streams (the link's rate for the inputs of one call)."""
+    import torch
+    h = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    d = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    ss = [torch.cuda.Stream(device=dev) for _ in range(streams)]
+    main = torch.cuda.current_stream(dev)
+
+    def once():
+        ev0 = torch.cuda.Event()
+        ev0.record(main)
+        for i, st in enumerate(ss):
+            st.wait_event(ev0)
+            a, b = nbytes * i // streams, nbytes * (i + 1) // streams
+            with torch.cuda.stream(st):
+                d[a:b].copy_(h[a:b], non_blocking=True)
+        for st in ss:
+            e = torch.cuda.Event()
+            e.record(st)
+            main.wait_event(e)
+
+    once()
+    torch.cuda.synchronize(dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(main)
+    for _ in range(5):
+        once()
+    b.record(main)
+    torch.cuda.synchronize(dev)
+    rate = 5 * nbytes / (a.elapsed_time(b) / 1e3) / 1e9
+    del h, d
+    return rate
+
+
+CONFIG_SWEEP = ["c1", "c2", "c3", "c4"]
+
+
+def run_ours(args, w, desc):
+    import torch
+    import torch.distributed as dist
+    from spec_verification_gb300 import build
+    from spec_verification_gb300.runner import DeviceRun
+
+    world, rank, local = dist_setup()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    build.build()
+    verify = w.is_verify
+    K, Wm = args.steps, args.warmup
+    run, ms_max, stages, ck, info = time_device(args, w, dev, world, K, Wm, tile=args.tile)
+    R, call_bytes, l2, G, NG = info["R"], info["call_bytes"], info["l2"], info["G"], info["NG"]
+
+    # end to end: inputs from pinned host memory, tokens back, every step;
+    # the streamed inputs are copied in row ranges over 4 copy streams
     e2e = None
     if not args.no_e2e:
         hrun = DeviceRun(w, device=str(dev), candidates=False, tile=args.tile, pinned_host=True)
@@ -460,44 +541,68 @@ def run_ours(args, w, desc):
                 "row_status": torch.empty(hrun.row_status.shape, dtype=torch.int32, pin_memory=True)}
         if verify:
             outs["num_accepted"] = torch.empty(hrun.num_accepted.shape, dtype=torch.int32, pin_memory=True)
+        stream = torch.cuda.Stream(device=dev)
+        copy_streams = [torch.cuda.Stream(device=dev) for _ in range(4)]
+        up_ev = [torch.cuda.Event() for _ in range(len(copy_streams) + 1)]
 
         def e2e_step():
-            hrun.upload(non_blocking=True)
-            hrun()
-            outs["tokens"].copy_(hrun.tokens, non_blocking=True)
-            outs["row_status"].copy_(hrun.row_status, non_blocking=True)
-            if verify:
-                outs["num_accepted"].copy_(hrun.num_accepted, non_blocking=True)
+            hrun.upload_split(stream, copy_streams, up_ev)
+            with torch.cuda.stream(stream):
+                hrun(stream=stream)
+                outs["tokens"].copy_(hrun.tokens, non_blocking=True)
+                outs["row_status"].copy_(hrun.row_status, non_blocking=True)
+                if verify:
+                    outs["num_accepted"].copy_(hrun.num_accepted, non_blocking=True)
 
-        with torch.cuda.stream(stream):
-            for _ in range(2):
-                e2e_step()
+        for _ in range(2):
+            e2e_step()
         stream.synchronize()
         if world > 1:
             dist.barrier()
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(stream):
-            a.record(stream)
-            for _ in range(E):
-                e2e_step()
-            b.record(stream)
+        a.record(stream)
+        for _ in range(E):
+            e2e_step()
+        b.record(stream)
         torch.cuda.synchronize(dev)
         ems = max_over_ranks(a.elapsed_time(b), world, dev)
+        h2d = hrun.input_bytes()
         e2e = {"value": whole_job_rate(world, w.B, E, ems), "unit": "rows/s",
-               "h2d_bytes_per_step": hrun.input_bytes(), "d2h_bytes_per_step": hrun.output_bytes(),
-               "steps": E, "ms_per_step": ems / E}
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": hrun.output_bytes(),
+               "steps": E, "ms_per_step": ems / E, "h2d_gbs": h2d / (ems / E / 1e3) / 1e9,
+               "copy_streams": len(copy_streams),
+               "plain_h2d_copy_gbs": {"1_stream": h2d_copy_rate(dev, h2d, 1), "4_streams": h2d_copy_rate(dev, h2d, 4)},
+               "note": "h2d_gbs: the step's input bytes over the step time; plain_h2d_copy_gbs: a pinned host -> "
+                       "device copy of the same bytes alone, the link's rate (the bound on e2e)"}
         del hrun
 
     diag = run.diag()
     peak, peak_kind = read_peaks()
     tile = run.plan.tile
-    alg1 = stage1_alg_bytes(w, tile, run.plan.stage1_ctas)
-    t1 = statistics.mean(st1) / 1e3
-    achieved = alg1 / t1 / 1e9
-    traffic = profiled_traffic(args.workload)
-    counted = w.counted_bytes(8192)  # the metric's definition: staging of 8192-token tiles
+    roof, hbm = roofline_of(w, run, stages, ms_max, K, peak, peak_kind, profiled_traffic(args.workload))
     value = whole_job_rate(world, w.B, K, ms_max)
+    n_ctas, n_tiles = run.plan.stage1_ctas, run.plan.num_tiles
+    del run
+    torch.cuda.empty_cache()
+
+    # the other configurations, each timed the same way (graph replays,
+    # resident inputs larger than L2, per-kernel events, clocks sampled)
+    configs = None
+    if not args.no_configs and args.workload == "c5":
+        configs = {}
+        K2 = max(10, min(K, 500) // 10 * 10)
+        for name in CONFIG_SWEEP:
+            wc, dc = workload(name)
+            rc_, msc, stc, ckc, _ = time_device(args, wc, dev, world, K2, max(Wm, 3), tile=args.tile)
+            roofc, hbmc = roofline_of(wc, rc_, stc, msc, K2, peak, peak_kind, profiled_traffic(name))
+            configs[name] = {"workload": dc, "value": whole_job_rate(world, wc.B, K2, msc), "unit": "rows/s",
+                             "ms_per_step": msc / K2, "steps": K2, "stages_us": stc, "roofline": roofc,
+                             "hbm": hbmc, "clocks": ckc, "positions": wc.n_positions, "V": wc.V,
+                             "dtype": "f32" if wc.dtype == "f32" else "bf16"}
+            del rc_
+            torch.cuda.empty_cache()
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
         cpu = cpu_baseline(w, args.workload, args.cpu_seconds)
@@ -507,19 +612,15 @@ def run_ours(args, w, desc):
             "ms_per_step": ms_max / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f32" if w.dtype == "f32" else "bf16", "data": "synthetic",
             "config": {"workload": desc, "name": args.workload, "B": w.B, "V": w.V,
-                       "positions": w.n_positions, "tile": tile, "tiles_per_row": run.plan.num_tiles,
+                       "positions": w.n_positions, "tile": tile, "tiles_per_row": n_tiles,
+                       "stage1_ctas": n_ctas,
                        "l2": f"inputs larger than L2: {R} resident copies walked in turn "
                              f"({R * call_bytes / 1e6:.0f} MB against {l2 / 1e6:.0f} MB of L2)",
                        "graph": f"{G} calls per CUDA graph ({NG} graphs over the copies), {K // G} replays, "
                                 f"the last with per-kernel events", "parallelism": f"replicas{world}"},
-            "roofline": {"bound": "hbm", "kernel": "stage1", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "peak_kind": peak_kind,
-                         "traffic": traffic, "alg_bytes_per_launch": alg1},
-            "stages_us": {"stage1": 1e3 * statistics.mean(st1), "stage2": 1e3 * statistics.mean(st2),
-                          "residual": 1e3 * statistics.mean(st3) if verify else 0.0},
-            "hbm": {"counted_bytes_per_call": counted, "counted_gbs": counted / (ms_max / K / 1e3) / 1e9,
-                    "counted_frac": counted / (ms_max / K / 1e3) / 1e9 / peak,
-                    "note": "counted = logits + bitmask + draft probs + staging write and read of 8192-token tiles per call"},
+            "roofline": roof,
+            "stages_us": stages,
+            "hbm": hbm,
             "clocks": ck,
             "e2e": e2e,
             "gpu_launches": K * (3 if verify else 2),
@@ -529,6 +630,7 @@ def run_ours(args, w, desc):
             # (nonzero: the run's results are not valid)
             "self_check": {"stage_fallbacks": int(diag[0]), "buffer_compactions": int(diag[4]),
                            "copy_timeouts": int(diag[3])},
+            "configs": configs,
             "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)
@@ -548,7 +650,20 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-configs", action="store_true",
+                    help="time only the main workload (by default a c5 run also times c1-c4)")
     args = ap.parse_args()
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        # one process per GPU: relaunch under torch.distributed.run
+        import socket
+        with socket.socket() as sk:
+            sk.bind(("127.0.0.1", 0))
+            port = sk.getsockname()[1]
+        cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={args.gpus}",
+               "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.abspath(__file__)] + sys.argv[1:]
+        os.execv(sys.executable, cmd)
+    if "WORLD_SIZE" in os.environ and int(os.environ["WORLD_SIZE"]) != args.gpus:
+        raise SystemExit(f"--gpus {args.gpus} but WORLD_SIZE={os.environ['WORLD_SIZE']}")
     if args.impl == "ours":
         args.warmup = max(args.warmup, 3)
     w, desc = workload(args.workload)

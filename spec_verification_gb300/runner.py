@@ -116,6 +116,30 @@ class DeviceRun:
         for k, v in self.host.items():
             self.d[k].copy_(v, non_blocking=non_blocking)
 
+    def upload_split(self, main, copy_streams, events):
+        """Host -> device copy of every input with the streamed tensors
+        (logits, draft probabilities) cut into row ranges, one per copy
+        stream, so that several copies run at once; the small inputs go on
+        `main`, which then waits for every copy stream.  events: one started
+        event plus one per copy stream (torch.cuda.Event, reused per call)."""
+        import torch
+        events[0].record(main)
+        for st in copy_streams:
+            st.wait_event(events[0])
+        for k, v in self.host.items():
+            if k in ("logits", "draft_probs") and v.dim() == 2 and v.shape[0] >= len(copy_streams):
+                n = v.shape[0]
+                for i, st in enumerate(copy_streams):
+                    r0, r1 = n * i // len(copy_streams), n * (i + 1) // len(copy_streams)
+                    with torch.cuda.stream(st):
+                        self.d[k][r0:r1].copy_(v[r0:r1], non_blocking=True)
+            else:
+                with torch.cuda.stream(main):
+                    self.d[k].copy_(v, non_blocking=True)
+        for i, st in enumerate(copy_streams):
+            events[i + 1].record(st)
+            main.wait_event(events[i + 1])
+
     def input_bytes(self) -> int:
         return sum(v.numel() * v.element_size() for v in self.host.values())
 

@@ -152,7 +152,7 @@ def test_run_ours_walks_every_copy(monkeypatch, capsys):
                             lambda d, l2=l2: type("Props", (), {"L2_cache_size": l2})())
         for w, K in cases:
             _FakeRun.used = []
-            args = argparse.Namespace(steps=K, warmup=3, tile=0, no_e2e=True, no_cpu=True, workload="c2",
+            args = argparse.Namespace(steps=K, warmup=3, tile=0, no_e2e=True, no_cpu=True, workload="c2", no_configs=True,
                                       cpu_seconds=1.0, e2e_steps=3)
             bench.run_ours(args, w, "test workload")
             line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
