@@ -61,9 +61,14 @@ class DeviceRun:
 
     def __init__(self, w: Workload, device: str = "cuda:0", tile: int = 0, max_positions: int | None = None,
                  candidates: bool = True, tokens_stride: int | None = None, pinned_host: bool = False,
-                 one_hot_drafts: bool = False):
+                 one_hot_drafts: bool = False, guard_bytes: int = 0):
         import torch
         self.w = w
+        # guard_bytes > 0: every output buffer and the workspace sit inside a
+        # larger allocation whose bands of guard_bytes before and after hold
+        # GUARD; guards_intact() reports the buffers whose bands changed
+        self.guard_bytes = guard_bytes
+        self._guarded = {}
         self.dev = torch.device(device)
         self.verify = w.is_verify
         # drafts without probabilities: nothing of q is uploaded; the library gets NULL
@@ -98,18 +103,44 @@ class DeviceRun:
         i32 = torch.int32
         if self.verify:
             ts = tokens_stride if tokens_stride is not None else w.max_gamma + 1
-            self.tokens = torch.full((w.B, ts), -1, dtype=i32, device=self.dev)
-            self.num_accepted = torch.zeros(w.B, dtype=i32, device=self.dev)
+            self.tokens = self._buffer("tokens", (w.B, ts), i32, -1)
+            self.num_accepted = self._buffer("num_accepted", (w.B,), i32, 0)
         else:
-            self.tokens = torch.full((w.B,), -1, dtype=i32, device=self.dev)
+            self.tokens = self._buffer("tokens", (w.B,), i32, -1)
             self.num_accepted = None
-        self.row_status = torch.zeros(w.B, dtype=i32, device=self.dev)
+        self.row_status = self._buffer("row_status", (w.B,), i32, 0)
         self.cand_ids = self.cand_probs = self.num_kept = None
         if candidates:
-            self.cand_ids = torch.full((npos, native.K), -1, dtype=i32, device=self.dev)
-            self.cand_probs = torch.zeros((npos, native.K), dtype=torch.float32, device=self.dev)
-            self.num_kept = torch.zeros(npos, dtype=i32, device=self.dev)
-        self.workspace = torch.zeros(self.plan.workspace_bytes, dtype=torch.uint8, device=self.dev)
+            self.cand_ids = self._buffer("cand_ids", (npos, native.K), i32, -1)
+            self.cand_probs = self._buffer("cand_probs", (npos, native.K), torch.float32, 0)
+            self.num_kept = self._buffer("num_kept", (npos,), i32, 0)
+        self.workspace = self._buffer("workspace", (self.plan.workspace_bytes,), torch.uint8, 0)
+
+    GUARD = 0xA5
+
+    def _buffer(self, name, shape, dtype, fill):
+        """A device tensor of `shape`, filled with `fill`, inside guard bands
+        when guard_bytes > 0."""
+        import torch
+        if not self.guard_bytes:
+            return torch.full(shape, fill, dtype=dtype, device=self.dev)
+        n = int(np.prod(shape)) * torch.empty((), dtype=dtype).element_size()
+        g = self.guard_bytes
+        raw = torch.full((n + 2 * g,), self.GUARD, dtype=torch.uint8, device=self.dev)
+        t = raw[g:g + n].view(dtype).view(shape)
+        t.fill_(fill)
+        self._guarded[name] = (raw, n)
+        return t
+
+    def guards_intact(self) -> list:
+        """Names of the buffers whose guard bands no longer hold GUARD."""
+        bad = []
+        for name, (raw, n) in self._guarded.items():
+            g = self.guard_bytes
+            h = raw.cpu().numpy()
+            if np.any(h[:g] != self.GUARD) or np.any(h[g + n:] != self.GUARD):
+                bad.append(name)
+        return bad
 
     def upload(self, non_blocking: bool = True):
         """Host -> device copy of every input (pinned host buffers)."""
