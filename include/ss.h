@@ -273,9 +273,12 @@ ss_status ss_verify(const void* target_logits, const void* draft_probs, const in
  * and params->workspace_bytes are ignored.  The scratch is a device array
  * of SS_NOALLOC_SCRATCH_BYTES inside libss.so, one per device per process:
  *  - the first call for a device (the plan's device) does the set-up: it
- *    looks the array's address up and clears it on params->stream.  Make
- *    that first call before any stream capture; under capture it returns
- *    SS_ERR_ARG;
+ *    looks the array's address up and clears it on params->stream;
+ *  - the address is looked up once per process and device: do not use this
+ *    call across a cudaDeviceReset of that device;
+ *  - the diagnostic counters (ss_workspace_diag_offset) of these calls live
+ *    in the library's array, which the caller never sees: they cannot be
+ *    read for this call;
  *  - the whole array starts at zero (set-up clears it); the counters in it
  *    must be zero when a call starts, and each completed call leaves them
  *    at zero again;
