@@ -36,7 +36,7 @@ if ROOT not in sys.path:
 
 METRIC = "rows/sec and achieved HBM GB/s (% of GB300 peak) per fused sample/verify call"
 FALLBACK_HBM_GBS = 6800.0
-STAGE1_SOURCES = ["spec_verification_gb300/csrc/ss_stage1.cu", "spec_verification_gb300/csrc/ss_common.cuh"]
+STAGE1_SOURCES = ["spec_verification_gb300/csrc/ss_stage1.cuh", "spec_verification_gb300/csrc/ss_common.cuh"]
 
 
 def workload(name: str):

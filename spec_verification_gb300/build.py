@@ -17,7 +17,8 @@ CSRC = PKG / "csrc"
 INCLUDE = ROOT / "include"
 BUILD = PKG / "_build"
 LIB = BUILD / "libss.so"
-SOURCES = ["ss_api.cu", "ss_stage1.cu", "ss_stage2.cu", "ss_residual.cu", "ss_noalloc.cu"]
+SOURCES = ["ss_api.cu", "ss_stage1.cu", "ss_stage1_f32.cu", "ss_stage1_bf16.cu", "ss_stage1_exact.cu",
+           "ss_stage2.cu", "ss_residual.cu", "ss_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -40,7 +41,7 @@ def flags() -> list:
 def _stale(obj: Path, src: Path) -> bool:
     if not obj.exists():
         return True
-    deps = [src, INCLUDE / "ss.h", CSRC / "ss_common.cuh", Path(__file__)]
+    deps = [src, INCLUDE / "ss.h", CSRC / "ss_common.cuh", CSRC / "ss_stage1.cuh", Path(__file__)]
     return any(d.exists() and d.stat().st_mtime > obj.stat().st_mtime for d in deps)
 
 

@@ -13,8 +13,9 @@
 #include "ss_common.cuh"
 
 namespace ss {
-const void* stage1_ptr(bool bf16, bool exact);
-void stage1_launch(bool bf16, bool exact, int grid, size_t smem, cudaStream_t st, const Params& P);
+const void* stage1_ptr(bool bf16, bool exact, bool aux, bool lse);
+void stage1_launch(bool bf16, bool exact, bool aux, bool lse, int grid, size_t smem, cudaStream_t st,
+                   const Params& P);
 __global__ void stage2_kernel(const Params P, int verify);
 __global__ void residual_kernel(const Params P);
 size_t stage1_smem_bytes(int BN, bool bf16, int nslot);
@@ -143,7 +144,7 @@ ss_status ss_plan_create(ss_plan** out, int32_t V, int32_t max_rows, int32_t max
   p->nslot = nslot;
   p->ldt = logits_dtype;
   p->qdt = q_dtype;
-  p->k1 = ss::stage1_ptr(bf16, false);
+  p->k1 = ss::stage1_ptr(bf16, false, true, true);
   p->exact = 0;
   p->spin_limit = kDefaultSpin;
   p->spin_hint_ns = 0u;
@@ -154,7 +155,10 @@ ss_status ss_plan_create(ss_plan** out, int32_t V, int32_t max_rows, int32_t max
     delete p;
     return fail(SS_ERR_UNSUPPORTED, "vocabulary too large for the stage-2 shared-memory merge");
   }
-  e = cudaFuncSetAttribute(p->k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p->smem1);
+  // every default-variant form of stage 1 (listed-token paths, normaliser)
+  for (int v = 0; v < 4 && e == cudaSuccess; ++v)
+    e = cudaFuncSetAttribute(ss::stage1_ptr(bf16, false, (v & 1) != 0, (v & 2) != 0),
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p->smem1);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(ss::stage2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p->smem2);
   if (e == cudaSuccess)
@@ -220,7 +224,7 @@ ss_status ss_plan_enable_exact(ss_plan* p, int enable) {
     DeviceGuard guard(p->device);
     // same launch bounds and shared memory as the default variant, so the
     // occupancy (and with it the stage-1 split) does not change
-    const cudaError_t e = cudaFuncSetAttribute(ss::stage1_ptr(p->ldt == SS_BF16, true),
+    const cudaError_t e = cudaFuncSetAttribute(ss::stage1_ptr(p->ldt == SS_BF16, true, true, true),
                                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p->smem1);
     if (e != cudaSuccess) return cuda_fail(e, "kernel attributes");
   }
@@ -333,7 +337,11 @@ ss_status launch(const ss_plan* pl, const ss::Params& P0, cudaStream_t st, bool 
       e = cudaEventRecordWithFlags(static_cast<cudaEvent_t>(ev[i]), st, rec_flags);
   };
   rec(0);
-  ss::stage1_launch(pl->ldt == SS_BF16, pl->exact != 0, pl->grid1, pl->smem1, st, P);
+  // the stage-1 form holding only the paths this call can take: listed-token
+  // paths when it passes a history or a bias list, the normaliser when it
+  // verifies drafts
+  ss::stage1_launch(pl->ldt == SS_BF16, pl->exact != 0, P.history != nullptr || P.bias != nullptr,
+                    P.cu_draft != nullptr, pl->grid1, pl->smem1, st, P);
   rec(1);
   ss::stage2_kernel<<<grid2, ss::stage2_threads(), smem2, st>>>(P, verify ? 1 : 0);
   rec(2);

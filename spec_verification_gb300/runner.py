@@ -10,6 +10,7 @@ from __future__ import annotations
 import numpy as np
 
 from . import native
+from . import workloads as W
 from .workloads import Workload
 
 
@@ -69,6 +70,10 @@ class DeviceRun:
         # GUARD; guards_intact() reports the buffers whose bands changed
         self.guard_bytes = guard_bytes
         self._guarded = {}
+        # the history and bias lists go to the library only when a row uses
+        # them (SS_PENALTY / SS_BIAS): a call without them runs the stage-1
+        # form that has no listed-token paths
+        self.uses_aux = bool(np.any(np.asarray(w.rows["flags"])[:w.B] & np.uint32(W.PENALTY | W.BIAS)))
         self.dev = torch.device(device)
         self.verify = w.is_verify
         # drafts without probabilities: nothing of q is uploaded; the library gets NULL
@@ -187,14 +192,15 @@ class DeviceRun:
             q = None if self.one_hot_drafts else (draft_probs if draft_probs is not None else d["draft_probs"])
             native.ss_verify(self.plan, lg, q, d["draft_ids"], d["rows"], d["cu_draft"], d["seeds"],
                              workspace=self.workspace, tokens=self.tokens, num_accepted=self.num_accepted,
-                             row_status=self.row_status, history=d["history"], bitmask=d.get("bitmask"),
-                             bias=d["bias"], hist_stride=self.hist_stride, bias_stride=self.bias_stride,
+                             row_status=self.row_status, history=d["history"] if self.uses_aux else None,
+                             bitmask=d.get("bitmask"), bias=d["bias"] if self.uses_aux else None, hist_stride=self.hist_stride, bias_stride=self.bias_stride,
                              cand_ids=self.cand_ids, cand_probs=self.cand_probs, num_kept=self.num_kept,
                              B=self.w.B, stream=stream, events=events)
         else:
             native.ss_sample(self.plan, lg, d["rows"], d["seeds"], workspace=self.workspace,
-                             tokens=self.tokens, row_status=self.row_status, history=d["history"],
-                             bitmask=d.get("bitmask"), bias=d["bias"], hist_stride=self.hist_stride,
+                             tokens=self.tokens, row_status=self.row_status,
+                             history=d["history"] if self.uses_aux else None,
+                             bitmask=d.get("bitmask"), bias=d["bias"] if self.uses_aux else None, hist_stride=self.hist_stride,
                              bias_stride=self.bias_stride, cand_ids=self.cand_ids,
                              cand_probs=self.cand_probs, num_kept=self.num_kept, B=self.w.B, stream=stream,
                              events=events)
