@@ -197,8 +197,9 @@ void ss_plan_destroy(ss_plan* plan);
 
 /* Device scratch a call needs: per-tile staging (B_pos * Z_v * 128 entries
  * of 8 bytes), per-tile metadata and per-row bookkeeping.  Must be zeroed
- * once before the first call (the library keeps its counters at zero
- * between calls). */
+ * once before the first call with a plan (the library keeps its counters at
+ * zero between calls); a workspace that held another plan's data must be
+ * zeroed again. */
 size_t ss_workspace_bytes(const ss_plan* plan);
 
 /* Tile size B_N and tile count Z_v the plan uses. */
@@ -281,7 +282,8 @@ ss_status ss_verify(const void* target_logits, const void* draft_probs, const in
  *    read for this call;
  *  - the whole array starts at zero (set-up clears it); the counters in it
  *    must be zero when a call starts, and each completed call leaves them
- *    at zero again;
+ *    at zero again; stage 2 always runs as its own launch here (the array
+ *    is shared by every plan, see ss_plan_set_fusion);
  *  - plans whose ss_workspace_bytes exceeds SS_NOALLOC_SCRATCH_BYTES are
  *    rejected with SS_ERR_UNSUPPORTED (use ss_sample with a workspace);
  *  - calls on the same device that overlap in time (different streams or
@@ -296,6 +298,18 @@ const char* ss_status_str(ss_status s);
 
 /* Text of the last error on the calling host thread ("" if none). */
 const char* ss_last_error(void);
+
+/* Where stage 2 (merge, epilogue, sampling / accept test, row walk) runs.
+ * mode 0 (the default) or 2: as its own launch after stage 1.  mode 1:
+ * inside the stage-1 launch whenever a position's lists fit its shared
+ * memory (otherwise its own launch) -- the CTA that writes a position's last
+ * segment list runs that position's stage 2 at once.  This saves a launch
+ * but not the position's stage-2 latency, which stays on the call's critical
+ * path; measured, it was not faster on the benchmark workloads, hence not
+ * the default.  Plans with exact sampling enabled never fuse.  Results do
+ * not depend on the mode.  Not thread-safe against calls using the plan.
+ * SS_ERR_ARG for a NULL plan or another mode. */
+ss_status ss_plan_set_fusion(ss_plan* plan, int32_t mode);
 
 /* Wait limit of stage 1's copy ring: a thread polls a ring slot's
  * completion at most `polls` times (0 restores the default, 2^22 polls)

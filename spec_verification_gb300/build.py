@@ -41,7 +41,7 @@ def flags() -> list:
 def _stale(obj: Path, src: Path) -> bool:
     if not obj.exists():
         return True
-    deps = [src, INCLUDE / "ss.h", CSRC / "ss_common.cuh", CSRC / "ss_stage1.cuh", Path(__file__)]
+    deps = [src, INCLUDE / "ss.h", CSRC / "ss_common.cuh", CSRC / "ss_stage1.cuh", CSRC / "ss_stage2.cuh", Path(__file__)]
     return any(d.exists() and d.stat().st_mtime > obj.stat().st_mtime for d in deps)
 
 

@@ -13,9 +13,12 @@
 #include "ss_common.cuh"
 
 namespace ss {
-const void* stage1_ptr(bool bf16, bool exact, bool aux, bool lse);
-void stage1_launch(bool bf16, bool exact, bool aux, bool lse, int grid, size_t smem, cudaStream_t st,
+const void* stage1_ptr(bool bf16, bool exact, bool aux, bool lse, bool fused);
+void stage1_launch(bool bf16, bool exact, bool aux, bool lse, bool fused, int grid, size_t smem, cudaStream_t st,
                    const Params& P);
+size_t stage1_fused_room(int BN, bool bf16, int nslot);
+ss_status sample_call(const void* logits, const ss_batch* params, const int32_t* history, const uint32_t* bitmask,
+                      const ss_bias_entry* bias, const uint64_t* seeds, ss_out* out, bool allow_fusion);
 __global__ void stage2_kernel(const Params P, int verify);
 __global__ void residual_kernel(const Params P);
 size_t stage1_smem_bytes(int BN, bool bf16, int nslot);
@@ -29,6 +32,8 @@ int residual_piece_tokens();
 struct ss_plan {
   int V, max_rows, max_positions, BN, Z, device, sms, nslot;
   int exact;  // stage 1 runs its exact-sampling variant
+  int fuse;   // stage 2 inside stage 1: 1 whenever it fits; 0 (the default) or 2 never
+  size_t fused_room;  // shared memory the fused form has for stage 2
   uint32_t spin_limit;  // polls of a stage-1 ring wait before it gives up
   uint32_t spin_hint_ns;  // suspend-time hint of each poll (0: the hardware's)
   ss_dtype ldt, qdt;
@@ -36,7 +41,7 @@ struct ss_plan {
   std::vector<int> grid2_by_cap;  // stage-2 grid for a shared-memory capacity of c lists (index c)
   size_t smem1, smem2, smem3;
   const void* k1;
-  size_t off_staging, off_tlse, off_tgm, off_tst, off_pos, off_rowc, off_rescnt, off_res, off_diag, ws_bytes;
+  size_t off_staging, off_tlse, off_tgm, off_tst, off_pos, off_rowc, off_rescnt, off_parr, off_res, off_diag, ws_bytes;
 };
 
 namespace {
@@ -144,8 +149,10 @@ ss_status ss_plan_create(ss_plan** out, int32_t V, int32_t max_rows, int32_t max
   p->nslot = nslot;
   p->ldt = logits_dtype;
   p->qdt = q_dtype;
-  p->k1 = ss::stage1_ptr(bf16, false, true, true);
+  p->k1 = ss::stage1_ptr(bf16, false, true, true, false);
   p->exact = 0;
+  p->fuse = 0;
+  p->fused_room = ss::stage1_fused_room(BN, bf16, nslot);
   p->spin_limit = kDefaultSpin;
   p->spin_hint_ns = 0u;
   p->smem1 = ss::stage1_smem_bytes(BN, bf16, nslot);
@@ -155,9 +162,9 @@ ss_status ss_plan_create(ss_plan** out, int32_t V, int32_t max_rows, int32_t max
     delete p;
     return fail(SS_ERR_UNSUPPORTED, "vocabulary too large for the stage-2 shared-memory merge");
   }
-  // every default-variant form of stage 1 (listed-token paths, normaliser)
-  for (int v = 0; v < 4 && e == cudaSuccess; ++v)
-    e = cudaFuncSetAttribute(ss::stage1_ptr(bf16, false, (v & 1) != 0, (v & 2) != 0),
+  // every default-variant form of stage 1 (listed-token paths, normaliser, fused stage 2)
+  for (int v = 0; v < 8 && e == cudaSuccess; ++v)
+    e = cudaFuncSetAttribute(ss::stage1_ptr(bf16, false, (v & 1) != 0, (v & 2) != 0, (v & 4) != 0),
                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p->smem1);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(ss::stage2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p->smem2);
@@ -203,7 +210,8 @@ ss_status ss_plan_create(ss_plan** out, int32_t V, int32_t max_rows, int32_t max
   p->off_tst = off;     off = align_up(off + PZ * 4, 256);
   p->off_pos = off;     off = align_up(off + P * sizeof(ss::PosResult), 256);
   p->off_rowc = off;    off = align_up(off + R * 4, 256);
-  p->off_rescnt = off;  off = align_up(off + 4, 256);
+  p->off_rescnt = off;  off = align_up(off + 8, 256);
+  p->off_parr = off;    off = align_up(off + P * 4, 256);
   p->off_res = off;     off = align_up(off + R * sizeof(ss::ResidEntry), 256);
   p->off_diag = off;    off = align_up(off + 8 * 4, 256);
   p->ws_bytes = off;
@@ -224,7 +232,7 @@ ss_status ss_plan_enable_exact(ss_plan* p, int enable) {
     DeviceGuard guard(p->device);
     // same launch bounds and shared memory as the default variant, so the
     // occupancy (and with it the stage-1 split) does not change
-    const cudaError_t e = cudaFuncSetAttribute(ss::stage1_ptr(p->ldt == SS_BF16, true, true, true),
+    const cudaError_t e = cudaFuncSetAttribute(ss::stage1_ptr(p->ldt == SS_BF16, true, true, true, false),
                                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p->smem1);
     if (e != cudaSuccess) return cuda_fail(e, "kernel attributes");
   }
@@ -232,6 +240,13 @@ ss_status ss_plan_enable_exact(ss_plan* p, int enable) {
   return SS_OK;
 }
 size_t ss_workspace_diag_offset(const ss_plan* p) { return p ? p->off_diag : 0; }
+
+ss_status ss_plan_set_fusion(ss_plan* p, int32_t mode) {
+  if (!p) return fail(SS_ERR_ARG, "plan is required");
+  if (mode < 0 || mode > 2) return fail(SS_ERR_ARG, "fusion mode must be 0 (default: off), 1 (on) or 2 (off)");
+  p->fuse = mode;
+  return SS_OK;
+}
 
 ss_status ss_plan_set_wait_limit(ss_plan* p, uint32_t polls, uint32_t suspend_ns) {
   if (!p) return fail(SS_ERR_ARG, "plan is required");
@@ -285,6 +300,7 @@ ss_status fill_common(const ss_plan* pl, const ss_batch* b, const void* logits, 
   P.ws.pos = reinterpret_cast<ss::PosResult*>(w + pl->off_pos);
   P.ws.row_count = reinterpret_cast<uint32_t*>(w + pl->off_rowc);
   P.ws.resid_count = reinterpret_cast<uint32_t*>(w + pl->off_rescnt);
+  P.ws.pos_arrive = reinterpret_cast<uint32_t*>(w + pl->off_parr);
   P.ws.resid = reinterpret_cast<ss::ResidEntry*>(w + pl->off_res);
   P.ws.diag = reinterpret_cast<uint32_t*>(w + pl->off_diag);
   P.out = *out;
@@ -317,7 +333,8 @@ int seg_cap_for(const ss_plan* pl, int B) {
   return cap;
 }
 
-ss_status launch(const ss_plan* pl, const ss::Params& P0, cudaStream_t st, bool verify, void* const* ev) {
+ss_status launch(const ss_plan* pl, const ss::Params& P0, cudaStream_t st, bool verify, void* const* ev,
+                 bool allow_fusion = true) {
   ss::Params P = P0;
   P.seg_cap = seg_cap_for(pl, P.B);
   P.exact_on = pl->exact;
@@ -339,11 +356,13 @@ ss_status launch(const ss_plan* pl, const ss::Params& P0, cudaStream_t st, bool 
   rec(0);
   // the stage-1 form holding only the paths this call can take: listed-token
   // paths when it passes a history or a bias list, the normaliser when it
-  // verifies drafts
+  // verifies drafts.  Stage 2 runs inside it (fused) when the plan asks for
+  // it and a position's lists fit the fused form's shared memory
+  const bool fused = allow_fusion && pl->fuse == 1 && pl->exact == 0 && smem2 <= pl->fused_room;
   ss::stage1_launch(pl->ldt == SS_BF16, pl->exact != 0, P.history != nullptr || P.bias != nullptr,
-                    P.cu_draft != nullptr, pl->grid1, pl->smem1, st, P);
+                    P.cu_draft != nullptr, fused, pl->grid1, pl->smem1, st, P);
   rec(1);
-  ss::stage2_kernel<<<grid2, ss::stage2_threads(), smem2, st>>>(P, verify ? 1 : 0);
+  if (!fused) ss::stage2_kernel<<<grid2, ss::stage2_threads(), smem2, st>>>(P, verify ? 1 : 0);
   rec(2);
   if (verify) ss::residual_kernel<<<pl->grid3, ss::kNT, pl->smem3, st>>>(P);
   rec(3);
@@ -360,6 +379,19 @@ extern "C" {
 ss_status ss_sample(const void* logits, const ss_batch* params, const int32_t* history,
                     const uint32_t* bitmask, const ss_bias_entry* bias, const uint64_t* seeds,
                     ss_out* out) {
+  return ss::sample_call(logits, params, history, bitmask, bias, seeds, out, true);
+}
+
+}  // extern "C"
+
+namespace ss {
+
+// ss_sample; allow_fusion = false keeps stage 2 as its own launch (the
+// no-alloc entry point, whose shared scratch may hold another plan's data
+// where this plan keeps the fused form's per-position counters).
+ss_status sample_call(const void* logits, const ss_batch* params, const int32_t* history,
+                      const uint32_t* bitmask, const ss_bias_entry* bias, const uint64_t* seeds, ss_out* out,
+                      bool allow_fusion) {
   if (!params || !out || !params->plan) return fail(SS_ERR_ARG, "params, out and plan are required");
   const ss_plan* pl = params->plan;
   if (params->B > pl->max_positions) return fail(SS_ERR_ARG, "B exceeds max_positions");
@@ -372,8 +404,12 @@ ss_status ss_sample(const void* logits, const ss_batch* params, const int32_t* h
   P.bias = bias;
   P.mask_tma = mask_rows_copyable(P);
   DeviceGuard guard(pl->device);
-  return launch(pl, P, static_cast<cudaStream_t>(params->stream), false, params->events);
+  return launch(pl, P, static_cast<cudaStream_t>(params->stream), false, params->events, allow_fusion);
 }
+
+}  // namespace ss
+
+extern "C" {
 
 ss_status ss_verify(const void* target_logits, const void* draft_probs, const int32_t* draft_ids,
                     const ss_batch* params, const uint64_t* seeds, ss_out* out) {

@@ -11,7 +11,8 @@
 // device (with that device current) looks up its address once with
 // cudaGetSymbolAddress, clears it on the call's stream, and every call then
 // hands that address to ss_sample as its workspace.  Nothing here allocates
-// device memory, and the launch sequence is exactly ss_sample's.
+// device memory, and the launch sequence is ss_sample's with stage 2 as its
+// own launch.
 #include <cuda_runtime.h>
 
 #include <cstdio>
@@ -22,6 +23,8 @@
 namespace ss {
 int plan_device(const ss_plan* p);
 void set_last_error(const char* msg);
+ss_status sample_call(const void* logits, const ss_batch* params, const int32_t* history, const uint32_t* bitmask,
+                      const ss_bias_entry* bias, const uint64_t* seeds, ss_out* out, bool allow_fusion);
 }  // namespace ss
 
 namespace {
@@ -103,5 +106,8 @@ extern "C" ss_status ss_sample_noalloc(const void* logits, const ss_batch* param
   ss_batch b = *params;
   b.workspace = scratch;
   b.workspace_bytes = kScratchBytes;
-  return ss_sample(logits, &b, history, bitmask, bias, seeds, out);
+  // stage 2 as its own launch: the scratch is shared by every plan, so the
+  // words where this plan keeps the fused form's per-position counters may
+  // hold another plan's lists
+  return ss::sample_call(logits, &b, history, bitmask, bias, seeds, out, false);
 }

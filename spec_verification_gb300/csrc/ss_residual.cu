@@ -196,6 +196,16 @@ __global__ void __launch_bounds__(kNT, 4) residual_kernel(const Params P) {
     }
     __syncthreads();
   }
+  // the queue is consumed: the last CTA to finish (every CTA has read the
+  // count by then) empties it for the next call
+  if (tid == 0) {
+    __threadfence();
+    const uint32_t done = atomicAdd(P.ws.resid_count + 1, 1u);
+    if (done == gridDim.x - 1u) {
+      P.ws.resid_count[0] = 0u;
+      P.ws.resid_count[1] = 0u;
+    }
+  }
 }
 
 size_t residual_smem_bytes(int BN) { return (size_t)BN * 2 + sizeof(S3Smem) + 16; }

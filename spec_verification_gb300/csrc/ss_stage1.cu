@@ -6,26 +6,26 @@
 
 namespace ss {
 
-const void* stage1_ptr_f32(bool aux, bool lse);
-const void* stage1_ptr_bf16(bool aux, bool lse);
+const void* stage1_ptr_f32(bool aux, bool lse, bool fused);
+const void* stage1_ptr_bf16(bool aux, bool lse, bool fused);
 const void* stage1_ptr_exact(bool bf16);
-void stage1_launch_f32(bool aux, bool lse, int grid, size_t smem, cudaStream_t st, const Params& P);
-void stage1_launch_bf16(bool aux, bool lse, int grid, size_t smem, cudaStream_t st, const Params& P);
+void stage1_launch_f32(bool aux, bool lse, bool fused, int grid, size_t smem, cudaStream_t st, const Params& P);
+void stage1_launch_bf16(bool aux, bool lse, bool fused, int grid, size_t smem, cudaStream_t st, const Params& P);
 void stage1_launch_exact(bool bf16, int grid, size_t smem, cudaStream_t st, const Params& P);
 
 // aux: the call passes a history or a bias list (rows may have penalties or
-// bias); lse: the call verifies drafts.  The exact-sampling variant holds
-// every path.
-const void* stage1_ptr(bool bf16, bool exact, bool aux, bool lse) {
+// bias); lse: the call verifies drafts; fused: stage 2 runs inside stage 1.
+// The exact-sampling variant holds every path and is never fused.
+const void* stage1_ptr(bool bf16, bool exact, bool aux, bool lse, bool fused) {
   if (exact) return stage1_ptr_exact(bf16);
-  return bf16 ? stage1_ptr_bf16(aux, lse) : stage1_ptr_f32(aux, lse);
+  return bf16 ? stage1_ptr_bf16(aux, lse, fused) : stage1_ptr_f32(aux, lse, fused);
 }
 
-void stage1_launch(bool bf16, bool exact, bool aux, bool lse, int grid, size_t smem, cudaStream_t st,
+void stage1_launch(bool bf16, bool exact, bool aux, bool lse, bool fused, int grid, size_t smem, cudaStream_t st,
                    const Params& P) {
   if (exact) stage1_launch_exact(bf16, grid, smem, st, P);
-  else if (bf16) stage1_launch_bf16(aux, lse, grid, smem, st, P);
-  else stage1_launch_f32(aux, lse, grid, smem, st, P);
+  else if (bf16) stage1_launch_bf16(aux, lse, fused, grid, smem, st, P);
+  else stage1_launch_f32(aux, lse, fused, grid, smem, st, P);
 }
 
 }  // namespace ss

@@ -50,6 +50,7 @@
 #include <type_traits>
 
 #include "ss_common.cuh"
+#include "ss_stage2.cuh"
 
 namespace ss {
 
@@ -94,8 +95,9 @@ struct __align__(16) S1Smem {
   float lm[kNT / 32];
   int cnt[3];  // appends of stage k go to cnt[k % 3]
   int dead, nan_flag, nf, out_cnt;
+  int s2_go;  // fused form: this CTA completed the position's last segment
   uint32_t rowbad;  // SS_ST_BAD_HIST / SS_ST_BAD_BIAS of the segment's row
-  int pad2[3];
+  int pad2[2];
   unsigned long long gmax;  // the segment's Gumbel-max so far (exact sampling)
 };
 
@@ -801,15 +803,46 @@ __device__ __forceinline__ Flagged staged_tokens(const uint16_t* aux, StageCtx s
 
 }  // namespace
 
+// The fused form: a segment's list and metadata are written; the CTA that
+// completes a position's last segment (an atomic count of the position's
+// written segments, released by a fence) runs the position's stage 2 at
+// once, in the candidate and scratch buffers, which are free between
+// segments (s2mem: P.seg_cap lists twice and the stage-2 state).  All
+// threads call; the barriers are uniform.
+template <bool FUSED>
+__device__ __forceinline__ void segment_done(const Params& P, int pos, const Split& sp, S1Smem& sm,
+                                             unsigned char* s2mem) {
+  if constexpr (FUSED) {
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      const int Z = P.Z;
+      const int nseg = seg_cta(sp, (long long)pos * Z + Z - 1, Z) - seg_cta(sp, (long long)pos * Z, Z) + 1;
+      const uint32_t old = atomicAdd(P.ws.pos_arrive + pos, 1u);
+      sm.s2_go = old == (uint32_t)(nseg - 1) ? 1 : 0;
+    }
+    __syncthreads();
+    if (sm.s2_go) {
+      __threadfence();
+      const int cap = P.seg_cap * kK;
+      unsigned long long* c2 = reinterpret_cast<unsigned long long*>(s2mem);
+      S2Smem& s2 = *reinterpret_cast<S2Smem*>(c2 + 2 * cap);
+      stage2_position<kNT>(P, P.cu_draft != nullptr ? 1 : 0, pos, sp, c2, c2 + cap, s2);
+      if (threadIdx.x == 0) P.ws.pos_arrive[pos] = 0u;
+    }
+  }
+}
+
 // Compile-time variants, chosen per call on the host (the fewer paths a
 // variant holds, the better its streaming loop compiles: measured, the
 // variant without the listed-token paths is 17 % faster on rows that use
 // none of them).  AUX: rows may have penalties or bias (the call passes a
 // history or a bias list).  LSE: the call verifies drafts, so untruncated
-// stochastic positions need the normaliser partials.
+// stochastic positions need the normaliser partials.  FUSED: stage 2 runs
+// inside this kernel (segment_done), for batches with few positions.
 // EXACT: the variant that also keeps each exact-sampling segment's
 // Gumbel-max; without it none of that code is in the streaming loop.
-template <bool BF16, bool EXACT, bool AUX, bool LSE>
+template <bool BF16, bool EXACT, bool AUX, bool LSE, bool FUSED>
 __global__ void __launch_bounds__(kNT, 2) stage1_kernel(const Params P) {
   constexpr int ESZ = BF16 ? 2 : 4;
   constexpr int VEC = BF16 ? 8 : 4;
@@ -832,9 +865,10 @@ __global__ void __launch_bounds__(kNT, 2) stage1_kernel(const Params P) {
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int V = P.V, Z = P.Z;
-  if (blockIdx.x == 0 && tid == 0) *P.ws.resid_count = 0u;  // residual queue of this call
   const int npos = num_positions(P);
   const Split sp = make_split(P, npos);
+  // fused form: verification rows past the plan's positions are reported here
+  if constexpr (FUSED) stage2_capacity_rows<kNT>(P, P.cu_draft != nullptr ? 1 : 0, blockIdx.x, gridDim.x);
   if (sp.T <= 0) return;
   if ((int)blockIdx.x >= sp.G) return;
   const long long g0 = seg_start(sp, blockIdx.x, Z), g1 = seg_start(sp, blockIdx.x + 1, Z);
@@ -1292,6 +1326,7 @@ __global__ void __launch_bounds__(kNT, 2) stage1_kernel(const Params P) {
       for (int q = tid; q < kK; q += kNT) stg[q] = 0ull;
       if (tid == 0) P.ws.tile_status[lslot] = 0u;
     }
+    segment_done<FUSED>(P, pos, sp, sm, smem_raw + L.cand);
     cp_async_wait_all();  // the next segment's bookkeeping
     __syncthreads();
     buf ^= 1;
@@ -1313,6 +1348,7 @@ __global__ void __launch_bounds__(kNT, 2) stage1_kernel(const Params P) {
         P.ws.tile_lse[ls] = make_float2(-INFINITY, 0.0f);
         P.ws.tile_gmax[ls] = 0ull;
       }
+      segment_done<FUSED>(P, p, sp, sm, smem_raw + L.cand);
     }
     if (tid == 0)
       for (int s = 0; s < NS && g + s < g1; ++s)

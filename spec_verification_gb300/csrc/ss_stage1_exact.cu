@@ -4,16 +4,16 @@
 
 namespace ss {
 
-template __global__ void stage1_kernel<false, true, true, true>(const Params);
-template __global__ void stage1_kernel<true, true, true, true>(const Params);
+template __global__ void stage1_kernel<false, true, true, true, false>(const Params);
+template __global__ void stage1_kernel<true, true, true, true, false>(const Params);
 
 const void* stage1_ptr_exact(bool bf16) {
-  return bf16 ? (const void*)stage1_kernel<true, true, true, true> : (const void*)stage1_kernel<false, true, true, true>;
+  return bf16 ? (const void*)stage1_kernel<true, true, true, true, false> : (const void*)stage1_kernel<false, true, true, true, false>;
 }
 
 void stage1_launch_exact(bool bf16, int grid, size_t smem, cudaStream_t st, const Params& P) {
-  if (bf16) stage1_kernel<true, true, true, true><<<grid, kNT, smem, st>>>(P);
-  else stage1_kernel<false, true, true, true><<<grid, kNT, smem, st>>>(P);
+  if (bf16) stage1_kernel<true, true, true, true, false><<<grid, kNT, smem, st>>>(P);
+  else stage1_kernel<false, true, true, true, false><<<grid, kNT, smem, st>>>(P);
 }
 
 }  // namespace ss

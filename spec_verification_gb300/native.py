@@ -54,7 +54,8 @@ class Out(C.Structure):
 
 EXPORTS = ["ss_plan_create", "ss_plan_destroy", "ss_workspace_bytes", "ss_plan_tile",
            "ss_plan_num_tiles", "ss_plan_stage1_ctas", "ss_sample", "ss_verify", "ss_status_str", "ss_last_error",
-           "ss_workspace_diag_offset", "ss_sample_noalloc", "ss_plan_enable_exact", "ss_plan_set_wait_limit"]
+           "ss_workspace_diag_offset", "ss_sample_noalloc", "ss_plan_enable_exact", "ss_plan_set_wait_limit",
+           "ss_plan_set_fusion"]
 
 _lib = None
 
@@ -86,6 +87,8 @@ def library() -> C.CDLL:
     L.ss_plan_enable_exact.restype = C.c_int
     L.ss_plan_set_wait_limit.argtypes = [C.c_void_p, C.c_uint32, C.c_uint32]
     L.ss_plan_set_wait_limit.restype = C.c_int
+    L.ss_plan_set_fusion.argtypes = [C.c_void_p, C.c_int32]
+    L.ss_plan_set_fusion.restype = C.c_int
     L.ss_sample.argtypes = [C.c_void_p, C.POINTER(Batch), C.c_void_p, C.c_void_p, C.c_void_p,
                             C.c_void_p, C.POINTER(Out)]
     L.ss_sample.restype = C.c_int
@@ -128,6 +131,11 @@ class Plan:
     def enable_exact(self, on: bool = True):
         """Run the exact-sampling variant of stage 1 (rows flagged SS_EXACT)."""
         _check(library().ss_plan_enable_exact(self._p, 1 if on else 0))
+
+    def set_fusion(self, mode: int):
+        """Where stage 2 runs: 1 inside the stage-1 launch whenever it fits,
+        0 (the default) or 2 as its own launch."""
+        _check(library().ss_plan_set_fusion(self._p, mode))
 
     def set_wait_limit(self, polls: int, suspend_ns: int = 0):
         """Polls of a stage-1 copy wait before the copy counts as lost (0:
