@@ -229,34 +229,47 @@ __device__ __forceinline__ void stage2_position(const Params& P, int verify, int
     }
     __syncthreads();
     // order: a candidate's place is the number of candidates above it
-    // (distinct values; empty slots (0) rank below every candidate)
+    // (distinct values; empty slots (0) rank below every candidate).  What a
+    // candidate needs that does not depend on its place is computed first,
+    // so that its latency overlaps the ordering: its fp64 softmax weight
+    // w_t = exp(l_t - l_0) against the largest logit l_0 (each warp finds
+    // it), its Gumbel noise (one Philox draw: the sample of a sampled / bonus
+    // position, or the truncated residual's of a draft) and, for a truncated
+    // draft position, its q.  Weights are unused for point masses.
     const unsigned long long v = tid < kK ? sm.top[tid] : 0ull;
-    const int nz = __syncthreads_count(v != 0ull);
-    if (v != 0ull) {
+    unsigned long long vmax = 0ull;
+#pragma unroll
+    for (int q = 0; q < kK / 32; ++q) {
+      const unsigned long long c = sm.top[q * 32 + lane];
+      vmax = c > vmax ? c : vmax;
+    }
+    vmax = warp_max_u64(vmax);
+    const float lz = key2f(pk_key(vmax));
+    const bool real = v != 0ull;
+    double wv = 0.0;
+    float gv = 0.0f, qvv = 0.0f;
+    if (real) {
+      const float lt = key2f(pk_key(v));
+      const int32_t tk = pk_tok(v);
+      if (rc.stoch && lt > -INFINITY && lz < INFINITY) wv = exp((double)lt - (double)lz);
+      if (rc.stoch && (!is_draft || rc.trunc))
+        gv = gumbel_of(philox_uniform(seed, (uint32_t)tk, position, (uint32_t)r, is_draft ? 2u : 0u));
+      if (is_draft && rc.stoch && rc.trunc)
+        qvv = P.q ? load_scalar(P.q, P.q_bf16, ((int64_t)c0 + j) * P.ld_q + tk) : (tk == sm.d ? 1.0f : 0.0f);
+    }
+    const int nz = __syncthreads_count(real);
+    if (real) {
       int rank = 0;
 #pragma unroll 8
       for (int u = 0; u < kK; ++u) rank += sm.top[u] > v ? 1 : 0;
       sm.srt[rank] = v;
+      sm.w[rank] = wv;
+      sm.g[rank] = gv;
+      sm.qv[rank] = qvv;
     }
-    if (tid < kK && tid >= nz) sm.srt[tid] = 0ull;
-    __syncthreads();
-    // softmax weights, one candidate per thread (the fp64 exp spread over
-    // four warps): w_t = exp(l_t - l_0) for finite l_t; unused for point masses
-    if (tid < kK) {
-      const unsigned long long c = sm.srt[tid];
-      const float lt = (tid < need && c != 0ull) ? key2f(pk_key(c)) : -INFINITY;
-      const float lz = key2f(pk_key(sm.srt[0]));
-      sm.w[tid] = (rc.stoch && lt > -INFINITY && lz < INFINITY) ? exp((double)lt - (double)lz) : 0.0;
-      // the candidate's Gumbel noise, one Philox draw per thread: the sample
-      // of a sampled / bonus position, or the truncated residual's of a draft
-      if (rc.stoch && (!is_draft || rc.trunc) && tid < need && c != 0ull)
-        sm.g[tid] = gumbel_of(philox_uniform(seed, (uint32_t)pk_tok(c), position, (uint32_t)r, is_draft ? 2u : 0u));
-      // a truncated draft position's residual needs q at every kept
-      // candidate: fetched here, one per thread, off the epilogue's chain
-      if (is_draft && rc.stoch && rc.trunc && tid < need && c != 0ull) {
-        const int32_t tk = pk_tok(c);
-        sm.qv[tid] = P.q ? load_scalar(P.q, P.q_bf16, ((int64_t)c0 + j) * P.ld_q + tk) : (tk == sm.d ? 1.0f : 0.0f);
-      }
+    if (tid < kK && tid >= nz) {
+      sm.srt[tid] = 0ull;
+      sm.w[tid] = 0.0;
     }
     if (tid == 0 && is_draft && rc.stoch) sm.u_acc = philox_uniform(seed, 0u, position, (uint32_t)r, 1u);
     __syncthreads();
