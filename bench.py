@@ -583,6 +583,9 @@ def run_ours(args, w, desc):
     roof, hbm = roofline_of(w, run, stages, ms_max, K, peak, peak_kind, profiled_traffic(args.workload))
     value = whole_job_rate(world, w.B, K, ms_max)
     n_ctas, n_tiles = run.plan.stage1_ctas, run.plan.num_tiles
+    uses_aux = bool(getattr(run, "uses_aux", False))
+    npos_bound = w.n_positions if verify else w.B
+    long_call = npos_bound * n_tiles >= 10 * n_ctas
     del run
     torch.cuda.empty_cache()
 
@@ -623,7 +626,10 @@ def run_ours(args, w, desc):
             "hbm": hbm,
             "clocks": ck,
             "e2e": e2e,
-            "gpu_launches": K * (3 if verify else 2),
+            # stage 1 (two launches for long calls with history or bias lists:
+            # the lean and the full form, one of which returns at once), stage
+            # 2, the residual pass of a verification call
+            "gpu_launches": K * ((3 if verify else 2) + (1 if uses_aux and long_call else 0)),
             # stage-1 counters over every call of the run: stages replaced by
             # their exact top-128, candidate buffers cut back to their exact
             # top-128, and bulk copies that did not land within the wait limit

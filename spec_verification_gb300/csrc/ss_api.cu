@@ -17,6 +17,8 @@ const void* stage1_ptr(bool bf16, bool exact, bool aux, bool lse, bool fused);
 void stage1_launch(bool bf16, bool exact, bool aux, bool lse, bool fused, int grid, size_t smem, cudaStream_t st,
                    const Params& P);
 size_t stage1_fused_room(int BN, bool bf16, int nslot);
+const void* stage1_lean_ptr(bool bf16);
+void stage1_launch_lean(bool bf16, int grid, size_t smem, cudaStream_t st, const Params& P);
 ss_status sample_call(const void* logits, const ss_batch* params, const int32_t* history, const uint32_t* bitmask,
                       const ss_bias_entry* bias, const uint64_t* seeds, ss_out* out, bool allow_fusion);
 __global__ void stage2_kernel(const Params P, int verify);
@@ -166,6 +168,8 @@ ss_status ss_plan_create(ss_plan** out, int32_t V, int32_t max_rows, int32_t max
   for (int v = 0; v < 8 && e == cudaSuccess; ++v)
     e = cudaFuncSetAttribute(ss::stage1_ptr(bf16, false, (v & 1) != 0, (v & 2) != 0, (v & 4) != 0),
                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p->smem1);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(ss::stage1_lean_ptr(bf16), cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p->smem1);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(ss::stage2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p->smem2);
   if (e == cudaSuccess)
@@ -359,8 +363,25 @@ ss_status launch(const ss_plan* pl, const ss::Params& P0, cudaStream_t st, bool 
   // verifies drafts.  Stage 2 runs inside it (fused) when the plan asks for
   // it and a position's lists fit the fused form's shared memory
   const bool fused = allow_fusion && pl->fuse == 1 && pl->exact == 0 && smem2 <= pl->fused_room;
-  ss::stage1_launch(pl->ldt == SS_BF16, pl->exact != 0, P.history != nullptr || P.bias != nullptr,
-                    P.cu_draft != nullptr, fused, pl->grid1, pl->smem1, st, P);
+  // A long call with history or bias lists launches the lean form
+  // (listed-token paths without count tables or normaliser) and then the full
+  // form: each CTA first checks the rows (call_needs_full) and exactly one of
+  // the two does the work, so the calls whose rows need neither path (the
+  // common case) stream through the leaner loop.  Measured: the mixed serving
+  // batch (76 stages per CTA) 6 % faster; a call of 3 stages per CTA 7 %
+  // slower (the second launch costs more than the leaner loop saves), hence
+  // the length test (at least 10 stages per CTA for the positions a call
+  // can have).
+  const bool aux = P.history != nullptr || P.bias != nullptr;
+  const long long npos_bound = verify ? pl->max_positions : std::min(P.B, pl->max_positions);
+  const bool dual = aux && pl->exact == 0 && !fused && npos_bound * pl->Z >= 10LL * pl->grid1;
+  P.dispatch = 0;
+  if (dual) {
+    P.dispatch = 1;
+    ss::stage1_launch_lean(pl->ldt == SS_BF16, pl->grid1, pl->smem1, st, P);
+    P.dispatch = 2;
+  }
+  ss::stage1_launch(pl->ldt == SS_BF16, pl->exact != 0, aux, P.cu_draft != nullptr, fused, pl->grid1, pl->smem1, st, P);
   rec(1);
   if (!fused) ss::stage2_kernel<<<grid2, ss::stage2_threads(), smem2, st>>>(P, verify ? 1 : 0);
   rec(2);

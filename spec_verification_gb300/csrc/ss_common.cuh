@@ -73,6 +73,7 @@ struct Params {
   int seg_cap;              // segment lists per position that stage 2's shared memory holds
   int exact_on;             // the plan runs the exact-sampling variant of stage 1
   int mask_tma;             // bitmask rows can be bulk-copied (16-byte aligned rows)
+  int dispatch;             // stage 1: 0 runs; 1 runs only if no row needs the full form, 2 only if one does
   uint32_t spin_limit;      // polls of a stage-1 ring wait before it gives up (the copy timeout)
   uint32_t spin_hint_ns;    // suspend-time hint of each poll in ns (0: the hardware's limit)
   Workspace ws;

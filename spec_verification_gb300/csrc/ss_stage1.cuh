@@ -833,6 +833,29 @@ __device__ __forceinline__ void segment_done(const Params& P, int pos, const Spl
   }
 }
 
+// Whether any row of the call needs the count-table or normaliser paths of
+// stage 1, which the lean form lacks: an untruncated stochastic row with
+// drafts (its draft positions need the full-vocabulary normaliser), or a row
+// with penalties or bias whose listed tokens at some position (history,
+// drafts before the position, bias entries) may exceed the hash table.  The
+// kernel's own per-position tests imply these (j < gamma, jn <= gamma).  All
+// threads call; every CTA reaches the same answer.
+__device__ __forceinline__ bool call_needs_full(const Params& P) {
+  const bool verify = P.cu_draft != nullptr;
+  int need = 0;
+  for (int r = threadIdx.x; r < P.B; r += kNT) {
+    const RowCtx rc = make_row(P.rows[r], P.hist_stride, P.bias_stride);
+    if (!rc.valid) continue;
+    const int gamma = verify ? __ldg(P.cu_draft + r + 1) - __ldg(P.cu_draft + r) : 0;
+    const bool pen_on = (rc.flags & SS_PENALTY) && P.history != nullptr;
+    const bool bias_on = (rc.flags & SS_BIAS) && P.bias != nullptr;
+    if (verify && gamma > 0 && rc.stoch && !rc.trunc) need = 1;
+    const int nflag_max = (pen_on ? rc.hist_len + gamma : 0) + (bias_on ? rc.n_bias : 0);
+    if ((pen_on || bias_on) && nflag_max > kHashMax) need = 1;
+  }
+  return __syncthreads_or(need) != 0;
+}
+
 // Compile-time variants, chosen per call on the host (the fewer paths a
 // variant holds, the better its streaming loop compiles: measured, the
 // variant without the listed-token paths is 17 % faster on rows that use
@@ -840,9 +863,13 @@ __device__ __forceinline__ void segment_done(const Params& P, int pos, const Spl
 // history or a bias list).  LSE: the call verifies drafts, so untruncated
 // stochastic positions need the normaliser partials.  FUSED: stage 2 runs
 // inside this kernel (segment_done), for batches with few positions.
+// STAGED = false (the lean form, with LSE = false): no per-stage count
+// tables; the host launches it beside the full form for calls with history
+// or bias lists, and P.dispatch makes exactly one of the two run
+// (call_needs_full).
 // EXACT: the variant that also keeps each exact-sampling segment's
 // Gumbel-max; without it none of that code is in the streaming loop.
-template <bool BF16, bool EXACT, bool AUX, bool LSE, bool FUSED>
+template <bool BF16, bool EXACT, bool AUX, bool LSE, bool FUSED, bool STAGED = true>
 __global__ void __launch_bounds__(kNT, 2) stage1_kernel(const Params P) {
   constexpr int ESZ = BF16 ? 2 : 4;
   constexpr int VEC = BF16 ? 8 : 4;
@@ -865,6 +892,7 @@ __global__ void __launch_bounds__(kNT, 2) stage1_kernel(const Params P) {
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int V = P.V, Z = P.Z;
+  if (P.dispatch != 0 && (P.dispatch == 2) != call_needs_full(P)) return;  // the other form serves this call
   const int npos = num_positions(P);
   const Split sp = make_split(P, npos);
   // fused form: verification rows past the plan's positions are reported here
@@ -989,7 +1017,7 @@ __global__ void __launch_bounds__(kNT, 2) stage1_kernel(const Params P) {
     const bool aux_on = AUX && rc.valid && (pen_on || bias_on);
     const int nflag = (pen_on ? rc.hist_len + jn : 0) + (bias_on ? rc.n_bias : 0);
     const bool hashed = aux_on && !lse_on && !gmax_on && nflag <= kHashMax;
-    const bool staged = aux_on && !hashed;
+    const bool staged = STAGED && aux_on && !hashed;
     const ss_bias_entry* brow = bias_on ? P.bias + (size_t)r * P.bias_stride : nullptr;
     const ss_bias_entry* bl = (bias_on && rc.n_bias <= kBiasPre) ? cb.bias : brow;
 

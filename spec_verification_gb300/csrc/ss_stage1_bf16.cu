@@ -6,6 +6,7 @@
 namespace ss {
 
 template __global__ void stage1_kernel<true, false, false, false, false>(const Params);
+template __global__ void stage1_kernel<true, false, true, false, false, false>(const Params);
 template __global__ void stage1_kernel<true, false, false, true, false>(const Params);
 template __global__ void stage1_kernel<true, false, true, false, false>(const Params);
 template __global__ void stage1_kernel<true, false, true, true, false>(const Params);
@@ -39,6 +40,13 @@ void stage1_launch_bf16(bool aux, bool lse, bool fused, int grid, size_t smem, c
     if (aux) lse ? launch_of<true, true, false>(grid, smem, st, P) : launch_of<true, false, false>(grid, smem, st, P);
     else lse ? launch_of<false, true, false>(grid, smem, st, P) : launch_of<false, false, false>(grid, smem, st, P);
   }
+}
+
+// The lean form: listed-token paths without count tables, no normaliser.
+const void* stage1_ptr_bf16_lean() { return (const void*)stage1_kernel<true, false, true, false, false, false>; }
+
+void stage1_launch_bf16_lean(int grid, size_t smem, cudaStream_t st, const Params& P) {
+  stage1_kernel<true, false, true, false, false, false><<<grid, kNT, smem, st>>>(P);
 }
 
 }  // namespace ss

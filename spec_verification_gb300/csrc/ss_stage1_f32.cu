@@ -6,6 +6,7 @@
 namespace ss {
 
 template __global__ void stage1_kernel<false, false, false, false, false>(const Params);
+template __global__ void stage1_kernel<false, false, true, false, false, false>(const Params);
 template __global__ void stage1_kernel<false, false, false, true, false>(const Params);
 template __global__ void stage1_kernel<false, false, true, false, false>(const Params);
 template __global__ void stage1_kernel<false, false, true, true, false>(const Params);
@@ -51,6 +52,13 @@ int stage1_max_slots() { return kMaxSlots; }
 size_t stage1_fused_room(int BN, bool bf16, int nslot) {
   const Layout L = layout(BN, bf16 ? 2 : 4, nslot);
   return L.out - L.cand;
+}
+
+// The lean form: listed-token paths without count tables, no normaliser.
+const void* stage1_ptr_f32_lean() { return (const void*)stage1_kernel<false, false, true, false, false, false>; }
+
+void stage1_launch_f32_lean(int grid, size_t smem, cudaStream_t st, const Params& P) {
+  stage1_kernel<false, false, true, false, false, false><<<grid, kNT, smem, st>>>(P);
 }
 
 }  // namespace ss
