@@ -214,7 +214,7 @@ ss_status ss_plan_create(ss_plan** out, int32_t V, int32_t max_rows, int32_t max
   p->off_tst = off;     off = align_up(off + PZ * 4, 256);
   p->off_pos = off;     off = align_up(off + P * sizeof(ss::PosResult), 256);
   p->off_rowc = off;    off = align_up(off + R * 4, 256);
-  p->off_rescnt = off;  off = align_up(off + 8, 256);
+  p->off_rescnt = off;  off = align_up(off + 12, 256);
   p->off_parr = off;    off = align_up(off + P * 4, 256);
   p->off_res = off;     off = align_up(off + R * sizeof(ss::ResidEntry), 256);
   p->off_diag = off;    off = align_up(off + 8 * 4, 256);

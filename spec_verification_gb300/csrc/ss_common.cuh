@@ -41,7 +41,8 @@ struct Workspace {
   uint32_t* tile_status;         // [P * Z] per segment SS_ST_* bits
   PosResult* pos;                // [P]
   uint32_t* row_count;           // [R] positions of the row done (stage-2 arrivals)
-  uint32_t* resid_count;         // [2] queued residual passes, residual CTAs done (the last resets both)
+  uint32_t* resid_count;         // [3] queued residual passes, residual CTAs done (the last resets both),
+                                 //     and whether the call needs the full stage-1 form (written by the lean form)
   uint32_t* pos_arrive;          // [P] fused form: segments of the position whose lists are written
   ResidEntry* resid;             // [R]
   uint32_t* diag;                // [8] diagnostic counters

@@ -892,7 +892,16 @@ __global__ void __launch_bounds__(kNT, 2) stage1_kernel(const Params P) {
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int V = P.V, Z = P.Z;
-  if (P.dispatch != 0 && (P.dispatch == 2) != call_needs_full(P)) return;  // the other form serves this call
+  // two forms launched for this call: the lean one (dispatch 1) checks the
+  // rows and publishes the answer for the full one (dispatch 2), which runs
+  // after it in stream order; exactly one of them does the work
+  if (P.dispatch == 1) {
+    const bool full = call_needs_full(P);
+    if (blockIdx.x == 0 && tid == 0) P.ws.resid_count[2] = full ? 1u : 0u;
+    if (full) return;
+  } else if (P.dispatch == 2) {
+    if (__ldcg(P.ws.resid_count + 2) == 0u) return;
+  }
   const int npos = num_positions(P);
   const Split sp = make_split(P, npos);
   // fused form: verification rows past the plan's positions are reported here
