@@ -586,6 +586,11 @@ def run_ours(args, w, desc):
     uses_aux = bool(getattr(run, "uses_aux", False))
     npos_bound = w.n_positions if verify else w.B
     long_call = npos_bound * n_tiles >= 10 * n_ctas
+    # stage 1 runs as two launches (lean and full form) for long calls with
+    # history or bias lists, except sampling calls whose lists fit the hash
+    # table (the lean form alone)
+    lists_fit = w.history.shape[1] + w.bias_tokens.shape[1] <= 512
+    two_forms = uses_aux and long_call and (verify or not lists_fit)
     del run
     torch.cuda.empty_cache()
 
@@ -629,7 +634,7 @@ def run_ours(args, w, desc):
             # stage 1 (two launches for long calls with history or bias lists:
             # the lean and the full form, one of which returns at once), stage
             # 2, the residual pass of a verification call
-            "gpu_launches": K * ((3 if verify else 2) + (1 if uses_aux and long_call else 0)),
+            "gpu_launches": K * ((3 if verify else 2) + (1 if two_forms else 0)),
             # stage-1 counters over every call of the run: stages replaced by
             # their exact top-128, candidate buffers cut back to their exact
             # top-128, and bulk copies that did not land within the wait limit

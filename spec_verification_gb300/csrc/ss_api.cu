@@ -18,6 +18,7 @@ void stage1_launch(bool bf16, bool exact, bool aux, bool lse, bool fused, int gr
                    const Params& P);
 size_t stage1_fused_room(int BN, bool bf16, int nslot);
 const void* stage1_lean_ptr(bool bf16);
+int stage1_hash_tokens();
 void stage1_launch_lean(bool bf16, int grid, size_t smem, cudaStream_t st, const Params& P);
 ss_status sample_call(const void* logits, const ss_batch* params, const int32_t* history, const uint32_t* bitmask,
                       const ss_bias_entry* bias, const uint64_t* seeds, ss_out* out, bool allow_fusion);
@@ -372,16 +373,26 @@ ss_status launch(const ss_plan* pl, const ss::Params& P0, cudaStream_t st, bool 
   // slower (the second launch costs more than the leaner loop saves), hence
   // the length test (at least 10 stages per CTA for the positions a call
   // can have).
+  // A sampling call whose history and bias strides together fit the hash
+  // table needs neither path (no drafts, and no row can list more tokens
+  // than the strides hold): the lean form alone serves it.
   const bool aux = P.history != nullptr || P.bias != nullptr;
   const long long npos_bound = verify ? pl->max_positions : std::min(P.B, pl->max_positions);
-  const bool dual = aux && pl->exact == 0 && !fused && npos_bound * pl->Z >= 10LL * pl->grid1;
+  const int listed_max = (P.history ? P.hist_stride : 0) + (P.bias ? P.bias_stride : 0);
+  const bool lean_only = aux && !verify && pl->exact == 0 && !fused && listed_max <= ss::stage1_hash_tokens();
+  const bool dual = aux && !lean_only && pl->exact == 0 && !fused && npos_bound * pl->Z >= 10LL * pl->grid1;
   P.dispatch = 0;
-  if (dual) {
-    P.dispatch = 1;
+  if (lean_only) {
     ss::stage1_launch_lean(pl->ldt == SS_BF16, pl->grid1, pl->smem1, st, P);
-    P.dispatch = 2;
+  } else {
+    if (dual) {
+      P.dispatch = 1;
+      ss::stage1_launch_lean(pl->ldt == SS_BF16, pl->grid1, pl->smem1, st, P);
+      P.dispatch = 2;
+    }
+    ss::stage1_launch(pl->ldt == SS_BF16, pl->exact != 0, aux, P.cu_draft != nullptr, fused, pl->grid1, pl->smem1, st,
+                      P);
   }
-  ss::stage1_launch(pl->ldt == SS_BF16, pl->exact != 0, aux, P.cu_draft != nullptr, fused, pl->grid1, pl->smem1, st, P);
   rec(1);
   if (!fused) ss::stage2_kernel<<<grid2, ss::stage2_threads(), smem2, st>>>(P, verify ? 1 : 0);
   rec(2);

@@ -49,6 +49,8 @@ size_t stage1_smem_bytes(int BN, bool bf16, int nslot) { return layout(BN, bf16 
 
 int stage1_max_slots() { return kMaxSlots; }
 
+int stage1_hash_tokens() { return kHashMax; }
+
 size_t stage1_fused_room(int BN, bool bf16, int nslot) {
   const Layout L = layout(BN, bf16 ? 2 : 4, nslot);
   return L.out - L.cand;
