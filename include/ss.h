@@ -336,7 +336,9 @@ ss_status ss_plan_set_wait_limit(ss_plan* plan, uint32_t polls, uint32_t suspend
  * expected); 2: residual passes over V; 3: stage-1 CTAs that gave up
  * waiting for a copy (their positions are left without candidates and
  * report SS_ST_COPY_TIMEOUT; not expected); 4: stage-1 candidate buffers cut
- * back to their exact top-128 after a histogram raise left too many.  They
+ * back to their exact top-128 after a histogram raise left too many; 5:
+ * stage-2 sample / bonus positions whose top-p or min-p cut point lay too
+ * close to its limit for the fp32 weights and was decided in fp64.  They
  * are cumulative and only cleared by the caller. */
 size_t ss_workspace_diag_offset(const ss_plan* plan);
 

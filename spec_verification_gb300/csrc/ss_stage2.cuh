@@ -42,6 +42,7 @@ struct S2Smem {
   unsigned long long top[kK];  // the selected candidates (unordered)
   unsigned long long srt[kK];  // the same, ordered
   double w[kK];                // exp(l_t - l_0) of the ordered candidates (stochastic rows)
+  float w32[kK];               // the same in fp32 (stochastic sample / bonus positions)
   float g[kK];                 // their Gumbel noise: sample (purpose 0) or residual (purpose 2)
   float qv[kK];                // their draft probability q (truncated draft positions)
   float u_acc;                 // the acceptance uniform (draft positions)
@@ -89,6 +90,12 @@ __device__ float prelude_single_warp(const Params& P, const RowCtx& rc, int pos,
   x = apply_temperature(x, rc);
   if (x != x) x = -INFINITY;
   return x;
+}
+
+__device__ __forceinline__ float warp_sum_f(float v) {
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) v += __shfl_xor_sync(0xffffffffu, v, d);
+  return v;
 }
 
 __device__ __forceinline__ int warp_sum_i(int v) {
@@ -247,11 +254,14 @@ __device__ __forceinline__ void stage2_position(const Params& P, int verify, int
     const float lz = key2f(pk_key(vmax));
     const bool real = v != 0ull;
     double wv = 0.0;
-    float gv = 0.0f, qvv = 0.0f;
+    float wf = 0.0f, gv = 0.0f, qvv = 0.0f;
     if (real) {
       const float lt = key2f(pk_key(v));
       const int32_t tk = pk_tok(v);
-      if (rc.stoch && lt > -INFINITY && lz < INFINITY) wv = exp((double)lt - (double)lz);
+      if (rc.stoch && lt > -INFINITY && lz < INFINITY) {
+        wv = exp((double)lt - (double)lz);
+        if (!is_draft) wf = expf(__fsub_rn(lt, lz));
+      }
       if (rc.stoch && (!is_draft || rc.trunc))
         gv = gumbel_of(philox_uniform(seed, (uint32_t)tk, position, (uint32_t)r, is_draft ? 2u : 0u));
       if (is_draft && rc.stoch && rc.trunc)
@@ -264,12 +274,14 @@ __device__ __forceinline__ void stage2_position(const Params& P, int verify, int
       for (int u = 0; u < kK; ++u) rank += sm.top[u] > v ? 1 : 0;
       sm.srt[rank] = v;
       sm.w[rank] = wv;
+      sm.w32[rank] = wf;
       sm.g[rank] = gv;
       sm.qv[rank] = qvv;
     }
     if (tid < kK && tid >= nz) {
       sm.srt[tid] = 0ull;
       sm.w[tid] = 0.0;
+      sm.w32[tid] = 0.0f;
     }
     if (tid == 0 && is_draft && rc.stoch) sm.u_acc = philox_uniform(seed, 0u, position, (uint32_t)r, 1u);
     __syncthreads();
@@ -300,56 +312,125 @@ __device__ __forceinline__ void stage2_position(const Params& P, int verify, int
       int nk = 0;
       double w[4] = {0.0, 0.0, 0.0, 0.0};
       double zk = 1.0;
+      float wf[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      float izkf = 1.0f;
+      bool f32 = false;  // the kept set and probabilities came from the fp32 weights
       if (no_finite) {
         nk = 0;
       } else if (point) {
         nk = 1;
       } else {
-        double ls = 0.0;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          w[k] = sm.w[4 * lane + k];
-          ls += w[k];
-        }
-        const double Zall = warp_sum_d(ls);
         int n2 = min(need, n_f);
         if ((rc.flags & SS_TOPK) && rc.top_k > 0) n2 = min(n2, rc.top_k);
-        if ((rc.flags & SS_TOPP) && rc.top_p < 1.0f) {
-          // t is kept iff the mass before it, sum_{u<t} w_u / Z, is below top_p:
-          // the exclusive prefix of w in candidate order against top_p * Z
-          double e[4], run = 0.0;
+        if (!is_draft) {
+          // A sample / bonus position takes its cut points from the fp32
+          // weights when they are certain: w32 is within (|l_t - l_0| 2^-24 +
+          // 2 ulp) of w relative, so the sums and prefixes are within 1.5e-5
+          // Z of the fp64 ones; a top-p prefix or a min-p weight closer than
+          // the stated margin to its limit sends the position to the fp64
+          // path below, which the oracle's fp64 decisions then match.
+          float lsf = 0.0f;
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
-            e[k] = run;
-            run += (4 * lane + k < need) ? w[k] : 0.0;
+            wf[k] = sm.w32[4 * lane + k];
+            lsf += wf[k];
           }
-          double incl = run;
+          const float Zf = warp_sum_f(lsf);
+          int m2 = n2;
+          bool unsure = false;
+          if ((rc.flags & SS_TOPP) && rc.top_p < 1.0f) {
+            float e[4], run = 0.0f;
 #pragma unroll
-          for (int d = 1; d < 32; d <<= 1) {
-            const double o = __shfl_up_sync(0xffffffffu, incl, d);
-            if (lane >= d) incl += o;
+            for (int k = 0; k < 4; ++k) {
+              e[k] = run;
+              run += (4 * lane + k < need) ? wf[k] : 0.0f;
+            }
+            float incl = run;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+              const float o = __shfl_up_sync(0xffffffffu, incl, d);
+              if (lane >= d) incl += o;
+            }
+            const float base = incl - run;
+            const float lim = rc.top_p * Zf;
+            const float tol = 2e-5f * Zf;
+            int c = 0;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              if (4 * lane + k < need) {
+                const float pre = base + e[k];
+                c += pre < lim ? 1 : 0;
+                unsure |= fabsf(pre - lim) <= tol;
+              }
+            }
+            m2 = min(m2, warp_sum_i(c));
           }
-          const double base = incl - run;
-          const double lim = (double)rc.top_p * Zall;
-          int c = 0;
+          if ((rc.flags & SS_MINP) && rc.min_p > 0.0f) {
+            int c = 0;
 #pragma unroll
-          for (int k = 0; k < 4; ++k) c += (4 * lane + k < need && base + e[k] < lim) ? 1 : 0;
-          n2 = min(n2, warp_sum_i(c));
+            for (int k = 0; k < 4; ++k) {
+              if (4 * lane + k < need) {
+                c += wf[k] >= rc.min_p ? 1 : 0;
+                unsure |= fabsf(wf[k] - rc.min_p) <= 2e-5f * fmaxf(wf[k], rc.min_p) + 1e-37f;
+              }
+            }
+            m2 = min(m2, warp_sum_i(c));
+          }
+          if (__any_sync(0xffffffffu, unsure)) {
+            if (lane == 0) atomicAdd(P.ws.diag + 5, 1u);
+          } else {
+            nk = max(1, m2);
+            float kz = 0.0f;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) kz += (4 * lane + k < nk) ? wf[k] : 0.0f;
+            izkf = 1.0f / warp_sum_f(kz);
+            f32 = true;
+          }
         }
-        if ((rc.flags & SS_MINP) && rc.min_p > 0.0f) {
-          // l_t - l_0 >= ln(min_p)  <=>  w_t = exp(l_t - l_0) >= min_p
-          int c = 0;
+        if (!f32) {
 #pragma unroll
-          for (int k = 0; k < 4; ++k) c += (4 * lane + k < need && w[k] >= (double)rc.min_p) ? 1 : 0;
-          n2 = min(n2, warp_sum_i(c));
+          for (int k = 0; k < 4; ++k) w[k] = sm.w[4 * lane + k];
+          double ls = 0.0;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) ls += w[k];
+          const double Zall = warp_sum_d(ls);
+          if ((rc.flags & SS_TOPP) && rc.top_p < 1.0f) {
+            // t is kept iff the mass before it, sum_{u<t} w_u / Z, is below top_p:
+            // the exclusive prefix of w in candidate order against top_p * Z
+            double e[4], run = 0.0;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              e[k] = run;
+              run += (4 * lane + k < need) ? w[k] : 0.0;
+            }
+            double incl = run;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+              const double o = __shfl_up_sync(0xffffffffu, incl, d);
+              if (lane >= d) incl += o;
+            }
+            const double base = incl - run;
+            const double lim = (double)rc.top_p * Zall;
+            int c = 0;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) c += (4 * lane + k < need && base + e[k] < lim) ? 1 : 0;
+            n2 = min(n2, warp_sum_i(c));
+          }
+          if ((rc.flags & SS_MINP) && rc.min_p > 0.0f) {
+            // l_t - l_0 >= ln(min_p)  <=>  w_t = exp(l_t - l_0) >= min_p
+            int c = 0;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) c += (4 * lane + k < need && w[k] >= (double)rc.min_p) ? 1 : 0;
+            n2 = min(n2, warp_sum_i(c));
+          }
+          nk = max(1, n2);
+          double kz = 0.0;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) kz += (4 * lane + k < nk) ? w[k] : 0.0;
+          zk = warp_sum_d(kz);
         }
-        nk = max(1, n2);
-        double kz = 0.0;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) kz += (4 * lane + k < nk) ? w[k] : 0.0;
-        zk = warp_sum_d(kz);
       }
-      const double izk = 1.0 / zk;
+      const double izk = (f32 || point || no_finite) ? 1.0 : 1.0 / zk;
       // candidate outputs
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
@@ -357,7 +438,7 @@ __device__ __forceinline__ void stage2_position(const Params& P, int verify, int
         if (cid) cid[t] = real[k] ? tok[k] : -1;
         if (cpr) {
           float pr = 0.0f;
-          if (t < nk) pr = point ? (t == 0 ? 1.0f : 0.0f) : (float)(w[k] * izk);
+          if (t < nk) pr = point ? (t == 0 ? 1.0f : 0.0f) : (f32 ? wf[k] * izkf : (float)(w[k] * izk));
           cpr[t] = pr;
         }
       }

@@ -543,3 +543,19 @@ def test_graph_replay_matches_eager():
     ora = O.verify(w2, tokens_stride=got["tokens"].shape[1])
     rep = parity.compare_verify(w2, got, ora)
     assert rep.ok(), rep
+
+
+def test_cut_points_on_the_boundary():
+    """Top-p and min-p cut points exactly on (or next to) their limits: equal
+    logits make the mass before the fifth candidate exactly half of the total
+    (top_p = 0.5), and min_p = exp(l_t - l_0) at a candidate.  The stage-2
+    epilogue decides such cut points in fp64 (dl-note, Top-p and Min-p)."""
+    V = 4096
+    x = np.full((6, V), -30.0, np.float32)
+    x[:, :10] = 2.0                      # ten equal logits: prefix before t is t / 10 of Z
+    x[3:, 10:20] = 2.0 - np.log(4.0, dtype=np.float32)   # weights exactly 1/4 of the top ones
+    w = sample_case(x, flags=[F.TOPP, F.TOPP, F.MINP, F.MINP, F.TOPP | F.MINP, F.TOPP],
+                    top_p=[0.5, 0.3, 0.0, 0.25, 0.5, 0.7], min_p=[0.0, 0.0, 0.5, 0.25, 0.25, 0.0],
+                    temperature=1.0)
+    gpu, ora, _ = check(w)
+    assert np.array_equal(gpu["num_kept"], ora["num_kept"])
