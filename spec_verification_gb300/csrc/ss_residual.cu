@@ -17,7 +17,8 @@ namespace ss {
 
 namespace {
 
-constexpr int kSub = 8 * kNT;  // tokens per work item: two groups of 4 per thread
+constexpr int kGroups = 2;                // groups of 4 tokens per thread in a work item (4: slower, spills)
+constexpr int kSub = 4 * kGroups * kNT;  // tokens per work item
 
 struct S3Smem {
   unsigned long long slots[kNT / 32];
@@ -48,6 +49,53 @@ __device__ __forceinline__ void prelude4(const Params& P, const RowCtx& rc, int 
     x = apply_temperature(x, rc);
     if (x != x) x = -INFINITY;
     out[k] = x;
+  }
+}
+
+// Four consecutive values i0..i0+3 of a row (fp32 or bf16 bits widened),
+// n_valid of them real (the rest 0): one 16- or 8-byte load when all four
+// are (rows are 16-byte aligned and i0 is a multiple of 4), else scalar.
+__device__ __forceinline__ void load4(const void* base, int bf16, int64_t row_off, int i0, int n_valid, float v[4]) {
+  if (n_valid >= 4) {
+    if (bf16) {
+      const uint2 u = __ldg(reinterpret_cast<const uint2*>(static_cast<const unsigned short*>(base) + row_off + i0));
+      v[0] = bf16_lo(u.x);
+      v[1] = bf16_hi(u.x);
+      v[2] = bf16_lo(u.y);
+      v[3] = bf16_hi(u.y);
+    } else {
+      const float4 f = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(base) + row_off + i0));
+      v[0] = f.x;
+      v[1] = f.y;
+      v[2] = f.z;
+      v[3] = f.w;
+    }
+    return;
+  }
+#pragma unroll
+  for (int k = 0; k < 4; ++k) v[k] = k < n_valid ? load_scalar(base, bf16, row_off + i0 + k) : 0.0f;
+}
+
+// prelude4 on loaded logits x (mask word mw of the group's tokens).
+__device__ __forceinline__ void prelude_loaded(const RowCtx& rc, int i0, int n_valid, uint32_t mw, bool masked,
+                                               const uint16_t* aux, int t0, const ss_bias_entry* brow, bool aux_on,
+                                               float x[4]) {
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int i = i0 + k;
+    if (k >= n_valid) {
+      x[k] = -INFINITY;
+      continue;
+    }
+    float v = x[k];
+    if (masked && ((mw >> (i & 31)) & 1u) == 0u) v = -INFINITY;
+    if (aux_on) {
+      const uint32_t a = aux[i - t0];
+      if (a != 0u) v = apply_penalty_bias(v, a & 0x7FFFu, (a & 0x8000u) != 0u, i, rc, brow);
+    }
+    v = apply_temperature(v, rc);
+    if (v != v) v = -INFINITY;
+    x[k] = v;
   }
 }
 
@@ -115,17 +163,37 @@ __global__ void __launch_bounds__(kNT, 4) residual_kernel(const Params P) {
     else __syncthreads();
 
     unsigned long long best = 0ull;
-    for (int i0 = t0 + 4 * tid; i0 < t0 + nt; i0 += 4 * kNT) {
-      float x[4];
-      prelude4(P, rc, pos, i0, min(4, t0 + nt - i0), aux, t0, brow, aux_on, x);
+    // the thread's kGroups groups of four tokens: every load of every group
+    // goes out before the first value is used
+    const bool masked = (rc.flags & SS_MASK) && P.bitmask;
+    float xg[kGroups][4], qg[kGroups][4];
+    uint32_t mw[kGroups];
+    int ig[kGroups], nv[kGroups];
+#pragma unroll
+    for (int gi = 0; gi < kGroups; ++gi) {
+      ig[gi] = t0 + 4 * tid + gi * 4 * kNT;
+      nv[gi] = min(4, t0 + nt - ig[gi]);
+      mw[gi] = 0xFFFFFFFFu;
+      if (nv[gi] > 0) {
+        load4(P.logits, P.logits_bf16, (int64_t)pos * P.ld, ig[gi], nv[gi], xg[gi]);
+        if (P.q) load4(P.q, P.q_bf16, qrow * P.ld_q, ig[gi], nv[gi], qg[gi]);
+        if (masked) mw[gi] = __ldg(P.bitmask + (size_t)pos * P.mask_words + (ig[gi] >> 5));
+      }
+    }
+#pragma unroll
+    for (int gi = 0; gi < kGroups; ++gi) {
+      if (nv[gi] <= 0) continue;
+      const int i0 = ig[gi];
+      float* x = xg[gi];
+      prelude_loaded(rc, i0, nv[gi], mw[gi], masked, aux, t0, brow, aux_on, x);
       float rr[4];
       bool any = false;
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         rr[k] = -1.0f;
-        if (x[k] > -INFINITY && i0 + k < t0 + nt) {
+        if (x[k] > -INFINITY && k < nv[gi]) {
           const float p = expf(x[k] - lse);
-          rr[k] = p - (P.q ? load_scalar(P.q, P.q_bf16, qrow * P.ld_q + i0 + k) : (i0 + k == dtok ? 1.0f : 0.0f));
+          rr[k] = p - (P.q ? qg[gi][k] : (i0 + k == dtok ? 1.0f : 0.0f));
           any |= rr[k] > 0.0f;
         }
       }
