@@ -32,7 +32,8 @@
 //    top-128;
 //  - history / draft / bias tokens need their count and bias entries, so they
 //    are kept out of that path: per segment they are listed in a hash table
-//    (which the rare appends consult) and their exact values, read straight
+//    (which the rare appends consult, when the appending thread's filter of
+//    its listed elements does not rule them out) and their exact values, read straight
 //    from HBM, are the segment's first candidates; very long histories (and
 //    verify positions that need the full-vocabulary normaliser) use a
 //    per-stage count table instead, appending those tokens as their stage
@@ -638,24 +639,46 @@ __device__ __forceinline__ int aux_bias_tok(const AuxRow& a, int e) {
 }
 
 // A thread's listed tokens (hash mode): their logits and mask words, loaded
-// at set-up and used once the first stage has been scanned.
+// at set-up and used once the first stage has been scanned; and the thread's
+// filter of the listed tokens among the elements it streams (own_bit).
 struct Listed {
   float raw[kHashMax / kNT];
   uint32_t mw[kHashMax / kNT];
+  uint32_t own;
 };
+
+// The streaming loop gives stage element li (li = ((ch * NV + v) * kNT + tid)
+// * VEC + jj, stages starting at multiples of B_N) to thread (li / VEC) % kNT.
+// Of the tokens a thread streams in a segment, token tok maps to bit
+// own_bit(tok) of a 32-bit filter: a hit whose bit is clear in the thread's
+// filter is no listed token, so the table is consulted only when it is set
+// (about one hit in 30 when a segment lists 512 tokens).  B_N / (kNT * VEC)
+// is a multiple of 32 / VEC, so the bit of an element is the same whether
+// counted from the token or from the stage.
+template <bool BF16>
+__device__ __forceinline__ int own_owner(int tok) {
+  constexpr int VEC = BF16 ? 8 : 4;
+  return (tok / VEC) % kNT;
+}
+template <bool BF16>
+__device__ __forceinline__ uint32_t own_bit(int i) {
+  constexpr int VEC = BF16 ? 8 : 4;
+  return 1u << (((i / (kNT * VEC)) * VEC + i % VEC) & 31);
+}
 
 // Segment set-up of a row with penalties or bias.  History / bias ids beyond
 // the vocabulary are reported in *rowbad.  In hash mode the segment's history,
 // draft and bias tokens inside [seg_lo, seg_hi) are listed in the hash table
 // (hkey / hval: count, bias flag in bit 31), then compacted to ftok / finfo
-// (*nf entries), and their logits (row_logits) and mask words (mask_row, or
-// none) are loaded.  All threads call; the barriers are uniform; the first one
-// also publishes the caller's counter resets.
+// (*nf entries), their logits (row_logits) and mask words (mask_row, or none)
+// are loaded, and each thread's filter (own_bit) is built in omask (kNT
+// words of scratch).  All threads call; the barriers are uniform; the first
+// one also publishes the caller's counter resets.
 template <bool BF16>
 __device__ __forceinline__ Listed seg_aux_setup(AuxRow a, bool hashed, int V, int seg_lo, int seg_hi, int* hkey,
                                              uint32_t* hval, int* ftok, uint32_t* finfo, int* nf,
                                              uint32_t* rowbad, const void* row_logits,
-                                             const uint32_t* mask_row) {
+                                             const uint32_t* mask_row, uint32_t* omask) {
   const int tid = threadIdx.x;
   Listed ls;
 #pragma unroll
@@ -663,11 +686,14 @@ __device__ __forceinline__ Listed seg_aux_setup(AuxRow a, bool hashed, int V, in
     ls.raw[k] = 0.0f;
     ls.mw[k] = 0xFFFFFFFFu;
   }
-  if (hashed)
+  ls.own = 0u;
+  if (hashed) {
     for (int q = tid; q < kHash; q += kNT) {
       hkey[q] = -1;
       hval[q] = 0u;
     }
+    omask[tid] = 0u;
+  }
   __syncthreads();
   // history / bias ids beyond the vocabulary are ignored and reported
   for (int h = tid; h < a.hist_len; h += kNT)
@@ -693,13 +719,17 @@ __device__ __forceinline__ Listed seg_aux_setup(AuxRow a, bool hashed, int V, in
   for (int s = tid; s < a.jn; s += kNT) insert(aux_draft(a, s), 1u, 0u);
   for (int e = tid; e < a.n_bias; e += kNT) insert(aux_bias_tok(a, e), 0u, 0x80000000u);
   __syncthreads();
-  for (int q = tid; q < kHash; q += kNT)
-    if (hkey[q] >= 0) {
+  for (int q = tid; q < kHash; q += kNT) {
+    const int tok = hkey[q];
+    if (tok >= 0) {
       const int i = atomicAdd(nf, 1);
-      ftok[i] = hkey[q];
+      ftok[i] = tok;
       finfo[i] = hval[q];
+      atomicOr(&omask[own_owner<BF16>(tok)], own_bit<BF16>(tok));
     }
+  }
   __syncthreads();
+  ls.own = omask[tid];
   const int nfl = *nf;
 #pragma unroll
   for (int k = 0; k < kHashMax / kNT; ++k) {
@@ -1051,7 +1081,8 @@ __global__ void __launch_bounds__(kNT, 2) stage1_kernel(const Params P) {
     if (aux_on)
       ls = seg_aux_setup<BF16>(ar, hashed, V, seg_lo, seg_hi, hkey, hval, ftok, finfo, &sm.nf, &sm.rowbad,
                                static_cast<const unsigned char*>(P.logits) + (size_t)pos * P.ld * ESZ,
-                               mask_on ? P.bitmask + (size_t)pos * P.mask_words : nullptr);
+                               mask_on ? P.bitmask + (size_t)pos * P.mask_words : nullptr,
+                               reinterpret_cast<uint32_t*>(tmp));  // tmp: free until the first stage's barrier
     else
       __syncthreads();
     const int nf = hashed ? sm.nf : 0;
@@ -1153,7 +1184,7 @@ __global__ void __launch_bounds__(kNT, 2) stage1_kernel(const Params P) {
                     nan_seen |= isn;
                     const unsigned long long pk = pack(isn ? kKeyNegInf : f2key(xv), (uint32_t)(t0 + li));
                     bool fl = false;
-                    if (hashed) fl = hash_find(hkey, t0 + li) >= 0;
+                    if (hashed) fl = (ls.own & own_bit<BF16>(li)) && hash_find(hkey, t0 + li) >= 0;
                     else if (staged) fl = aux[li] != 0u;
                     if (pk >= cutp && !fl) append(pk);
                   }
@@ -1194,7 +1225,7 @@ __global__ void __launch_bounds__(kNT, 2) stage1_kernel(const Params P) {
                 nan_seen |= isn;
                 const unsigned long long pk = pack(isn ? kKeyNegInf : f2key(xv), (uint32_t)(t0 + li));
                 bool fl = false;
-                if (hashed) fl = hash_find(hkey, t0 + li) >= 0;
+                if (hashed) fl = (ls.own & own_bit<BF16>(li)) && hash_find(hkey, t0 + li) >= 0;
                 else if (staged) fl = aux[li] != 0u;
                 if (pk >= cutp && !fl) append(pk);
               }
