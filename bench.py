@@ -454,7 +454,11 @@ def roofline_of(w, run, stages, ms_max, K, peak, peak_kind, traffic=None) -> tup
     """The stage-1 roofline and the whole call's counted-byte rate."""
     alg1 = stage1_alg_bytes(w, run.plan.tile, run.plan.stage1_ctas)
     achieved = alg1 / (stages["stage1"] / 1e6) / 1e9
-    roof = {"bound": "hbm", "kernel": "stage1", "achieved": achieved, "peak": peak, "unit": "GB/s",
+    # a call without a stage-2 launch ran stage 2 inside stage 1 (the fused
+    # form: stage 1, plus the residual pass of a verification call)
+    fused = run.plan.last_launches() == (2 if w.is_verify else 1)
+    roof = {"bound": "hbm", "kernel": "stage1 with stage 2 fused into it" if fused else "stage1",
+            "achieved": achieved, "peak": peak, "unit": "GB/s",
             "frac": achieved / peak, "peak_kind": peak_kind, "traffic": traffic, "alg_bytes_per_launch": alg1}
     counted = w.counted_bytes(8192)  # the metric's definition: staging of 8192-token tiles
     s_call = ms_max / K / 1e3
@@ -583,14 +587,9 @@ def run_ours(args, w, desc):
     roof, hbm = roofline_of(w, run, stages, ms_max, K, peak, peak_kind, profiled_traffic(args.workload))
     value = whole_job_rate(world, w.B, K, ms_max)
     n_ctas, n_tiles = run.plan.stage1_ctas, run.plan.num_tiles
-    uses_aux = bool(getattr(run, "uses_aux", False))
-    npos_bound = w.n_positions if verify else w.B
-    long_call = npos_bound * n_tiles >= 10 * n_ctas
-    # stage 1 runs as two launches (lean and full form) for long calls with
-    # history or bias lists, except sampling calls whose lists fit the hash
-    # table (the lean form alone)
-    lists_fit = w.history.shape[1] + w.bias_tokens.shape[1] <= 512
-    two_forms = uses_aux and long_call and (verify or not lists_fit)
+    # kernels per call, as the library recorded its launch decisions (one or
+    # two stage-1 forms, stage 2 unless fused, the residual pass of ss_verify)
+    launches_per_call = run.plan.last_launches()
     del run
     torch.cuda.empty_cache()
 
@@ -607,7 +606,8 @@ def run_ours(args, w, desc):
             configs[name] = {"workload": dc, "value": whole_job_rate(world, wc.B, K2, msc), "unit": "rows/s",
                              "ms_per_step": msc / K2, "steps": K2, "stages_us": stc, "roofline": roofc,
                              "hbm": hbmc, "clocks": ckc, "positions": wc.n_positions, "V": wc.V,
-                             "dtype": "f32" if wc.dtype == "f32" else "bf16"}
+                             "dtype": "f32" if wc.dtype == "f32" else "bf16",
+                             "gpu_launches": K2 * rc_.plan.last_launches()}
             del rc_
             torch.cuda.empty_cache()
 
@@ -631,10 +631,7 @@ def run_ours(args, w, desc):
             "hbm": hbm,
             "clocks": ck,
             "e2e": e2e,
-            # stage 1 (two launches for long calls with history or bias lists:
-            # the lean and the full form, one of which returns at once), stage
-            # 2, the residual pass of a verification call
-            "gpu_launches": K * ((3 if verify else 2) + (1 if two_forms else 0)),
+            "gpu_launches": K * launches_per_call,
             # stage-1 counters over every call of the run: stages replaced by
             # their exact top-128, candidate buffers cut back to their exact
             # top-128, and bulk copies that did not land within the wait limit

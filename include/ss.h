@@ -300,16 +300,30 @@ const char* ss_status_str(ss_status s);
 const char* ss_last_error(void);
 
 /* Where stage 2 (merge, epilogue, sampling / accept test, row walk) runs.
- * mode 0 (the default) or 2: as its own launch after stage 1.  mode 1:
- * inside the stage-1 launch whenever a position's lists fit its shared
- * memory (otherwise its own launch) -- the CTA that writes a position's last
- * segment list runs that position's stage 2 at once.  This saves a launch
- * but not the position's stage-2 latency, which stays on the call's critical
- * path; measured, it was not faster on the benchmark workloads, hence not
- * the default.  Plans with exact sampling enabled never fuse.  Results do
- * not depend on the mode.  Not thread-safe against calls using the plan.
- * SS_ERR_ARG for a NULL plan or another mode. */
+ * Fused: inside the stage-1 launch, where the CTA that writes a position's
+ * last segment list runs that position's stage 2 at once (only when a
+ * position's lists fit that launch's shared memory; otherwise, and
+ * unfused, stage 2 is its own launch after stage 1).  Fusing saves a launch
+ * and lets a position's stage 2 overlap the streaming of other positions,
+ * but it delays the rest of the fusing CTA's stage-1 range.
+ *  - mode 0 (the default): fused when the call passes no history and no
+ *    bias list and the positions it can have (B for ss_sample, the plan's
+ *    max_positions for ss_verify) span at least two stage-1 stages per
+ *    stage-1 CTA.  Calls with lists keep their lean / full stage-1 dispatch,
+ *    which the fused form does not have.
+ *  - mode 1: fused whenever the lists fit.
+ *  - mode 2: never.
+ * Plans with exact sampling enabled never fuse.  Results do not depend on
+ * the mode.  Not thread-safe against calls using the plan.  SS_ERR_ARG for a
+ * NULL plan or another mode. */
 ss_status ss_plan_set_fusion(ss_plan* plan, int32_t mode);
+
+/* Kernels launched by the most recent successful ss_sample / ss_verify /
+ * ss_sample_noalloc call with this plan (stage-1 forms, stage 2 unless
+ * fused, the residual pass of ss_verify); 0 before the first.  A host-side
+ * record of the launch decisions, for accounting; not thread-safe against
+ * calls using the plan. */
+int32_t ss_plan_last_launches(const ss_plan* plan);
 
 /* Wait limit of stage 1's copy ring: a thread polls a ring slot's
  * completion at most `polls` times (0 restores the default, 2^22 polls)

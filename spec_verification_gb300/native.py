@@ -55,7 +55,7 @@ class Out(C.Structure):
 EXPORTS = ["ss_plan_create", "ss_plan_destroy", "ss_workspace_bytes", "ss_plan_tile",
            "ss_plan_num_tiles", "ss_plan_stage1_ctas", "ss_sample", "ss_verify", "ss_status_str", "ss_last_error",
            "ss_workspace_diag_offset", "ss_sample_noalloc", "ss_plan_enable_exact", "ss_plan_set_wait_limit",
-           "ss_plan_set_fusion"]
+           "ss_plan_set_fusion", "ss_plan_last_launches"]
 
 _lib = None
 
@@ -89,6 +89,8 @@ def library() -> C.CDLL:
     L.ss_plan_set_wait_limit.restype = C.c_int
     L.ss_plan_set_fusion.argtypes = [C.c_void_p, C.c_int32]
     L.ss_plan_set_fusion.restype = C.c_int
+    L.ss_plan_last_launches.argtypes = [C.c_void_p]
+    L.ss_plan_last_launches.restype = C.c_int32
     L.ss_sample.argtypes = [C.c_void_p, C.POINTER(Batch), C.c_void_p, C.c_void_p, C.c_void_p,
                             C.c_void_p, C.POINTER(Out)]
     L.ss_sample.restype = C.c_int
@@ -134,8 +136,12 @@ class Plan:
 
     def set_fusion(self, mode: int):
         """Where stage 2 runs: 1 inside the stage-1 launch whenever it fits,
-        0 (the default) or 2 as its own launch."""
+        2 as its own launch, 0 (the default) by the call's shape."""
         _check(library().ss_plan_set_fusion(self._p, mode))
+
+    def last_launches(self) -> int:
+        """Kernels the most recent successful call with this plan launched."""
+        return int(library().ss_plan_last_launches(self._p))
 
     def set_wait_limit(self, polls: int, suspend_ns: int = 0):
         """Polls of a stage-1 copy wait before the copy counts as lost (0:

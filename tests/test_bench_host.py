@@ -111,7 +111,8 @@ class _FakeRun:
         self.d = {"logits": torch.zeros((n, w.V), dtype=torch.float32)}
         if w.is_verify:
             self.d["draft_probs"] = torch.zeros((int(w.cu_draft[-1]), w.V), dtype=torch.float32)
-        self.plan = type("P", (), {"tile": 8192, "stage1_ctas": 304, "num_tiles": -(-w.V // 8192)})()
+        self.plan = type("P", (), {"tile": 8192, "stage1_ctas": 304, "num_tiles": -(-w.V // 8192),
+                                   "last_launches": lambda self: 3 if w.is_verify else 2})()
         self._np = np
 
     def __call__(self, stream=None, logits=None, draft_probs=None, events=None):

@@ -214,6 +214,35 @@ def test_starting_cut_fallback_on_listed_maxima():
     assert d.diag()[0] > 0
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_listed_tokens_above_the_cut_in_later_stages(dtype):
+    # 48 rows x 16 tiles: segments of 3 stages, so most listed tokens are met
+    # by the streaming loop of a later stage.  400 history tokens and 16
+    # bias tokens per row carry the largest raw logits of the row but large
+    # penalties / negative bias (their processed values fall far below the
+    # top-128), and 8 more bias tokens are lifted into it: each hit on a
+    # listed token must be recognised (the thread's filter bit, then the
+    # table) and left to its exact value, or it would enter a list twice.
+    rng = np.random.default_rng(33)
+    B, V = 48, 131072
+    x = rng.standard_normal((B, V)).astype(np.float32)
+    hist = np.stack([rng.choice(V, 400, replace=False) for _ in range(B)]).astype(np.int32)
+    neg = np.stack([rng.choice(np.setdiff1d(np.arange(V), h), 24, replace=False) for h in hist]).astype(np.int32)
+    rows = np.arange(B)[:, None]
+    x[rows, hist] = 8.0
+    x[rows, neg[:, :16]] = 7.0
+    x[rows, neg[:, 16:]] = 0.0
+    bval = np.concatenate([np.full((B, 16), -50.0, np.float32), np.full((B, 8), 20.0, np.float32)], axis=1)
+    w = sample_case(x, flags=F.PENALTY | F.BIAS | F.TOPK, dtype=dtype, history=hist, bias_tokens=neg,
+                    bias_values=bval, rep=1.0, freq=0.0, pres=100.0, top_k=[16] * B,
+                    temperature=[1.0, 0.8] * (B // 2))
+    gpu, ora, _ = check(w)
+    # the lifted bias tokens lead every row, no penalised or lowered one is a candidate
+    for r in range(B):
+        assert set(gpu["cand_ids"][r][:8].tolist()) == set(neg[r, 16:].tolist())
+        assert not (set(gpu["cand_ids"][r].tolist()) & (set(hist[r].tolist()) | set(neg[r, :16].tolist())))
+
+
 def test_deterministic_repeat():
     w = W.sample_workload(25, 8, 60000, "bf16")
     from spec_verification_gb300.runner import DeviceRun
