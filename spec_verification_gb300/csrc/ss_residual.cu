@@ -4,7 +4,7 @@
 //
 // The row walk of stage 2 queues (row, rejected draft index, target position)
 // entries.  This kernel has a fixed launch shape (persistent CTAs) and loops
-// over (entry, 2048-token piece) items: each piece recomputes the processed
+// over (entry, piece) items: each piece recomputes the processed
 // logits with the stage-1 prelude, p_i = exp(l_i - LSE) with the LSE stage 2
 // assembled from the tiles' (max, sum exp) partials, r_i = p_i - q_i, and the
 // Gumbel-max score ln r_i + g_i (Philox purpose 2) over r_i > 0.  Pieces
@@ -137,9 +137,19 @@ __global__ void __launch_bounds__(kNT, 4) residual_kernel(const Params P) {
   const int tid = threadIdx.x;
   const int Z = P.Z, V = P.V;
   const int count = (int)__ldcg(P.ws.resid_count);
-  // items are (entry, kSub-token piece): an entry's pieces run on many CTAs,
-  // so a handful of rejections still spreads over the whole GPU
-  const int nsub = (V + kSub - 1) / kSub;
+  // items are (entry, piece): an entry's pieces run on many CTAs, so a
+  // handful of rejections still spreads over the whole GPU.  A piece is a
+  // multiple of kSub tokens (at most B_N, the aux table), as few as spread
+  // the entries over the grid in one round: pieces of kSub when the entries
+  // are few, longer ones (streamed kSub at a time, one prelude, reduction
+  // and arrival per piece) when more entries would need several rounds.
+  int psz = kSub;
+  if (count > 0) {
+    const int want = max(1, (int)gridDim.x / count);  // pieces per entry for one round
+    psz = (((V + want - 1) / want) + kSub - 1) / kSub * kSub;
+    psz = max(kSub, min(psz, P.BN / kSub * kSub));
+  }
+  const int nsub = (V + psz - 1) / psz;
   const long long total = (long long)count * nsub;
   for (long long item = blockIdx.x; item < total; item += gridDim.x) {
     const int e = (int)(item / nsub);
@@ -156,57 +166,60 @@ __global__ void __launch_bounds__(kNT, 4) residual_kernel(const Params P) {
     const bool bias_on = (rc.flags & SS_BIAS) && P.bias != nullptr;
     const bool aux_on = pen_on || bias_on;
     const ss_bias_entry* brow = bias_on ? P.bias + (size_t)r * P.bias_stride : nullptr;
-    const int t0 = piece * kSub;
-    const int nt = min(kSub, V - t0);
+    const int t0 = piece * psz;
+    const int nt = min(psz, V - t0);
     if (tid == 0) sm.last = 0;
     if (aux_on) build_aux(P, rc, r, j, t0, nt, aux, pen_on, bias_on, brow);
     else __syncthreads();
 
     unsigned long long best = 0ull;
-    // the thread's kGroups groups of four tokens: every load of every group
-    // goes out before the first value is used
     const bool masked = (rc.flags & SS_MASK) && P.bitmask;
-    float xg[kGroups][4], qg[kGroups][4];
-    uint32_t mw[kGroups];
-    int ig[kGroups], nv[kGroups];
+#pragma unroll 1
+    for (int s0 = t0; s0 < t0 + nt; s0 += kSub) {
+      // the thread's kGroups groups of four tokens of this kSub-token part:
+      // every load of every group goes out before the first value is used
+      float xg[kGroups][4], qg[kGroups][4];
+      uint32_t mw[kGroups];
+      int ig[kGroups], nv[kGroups];
 #pragma unroll
-    for (int gi = 0; gi < kGroups; ++gi) {
-      ig[gi] = t0 + 4 * tid + gi * 4 * kNT;
-      nv[gi] = min(4, t0 + nt - ig[gi]);
-      mw[gi] = 0xFFFFFFFFu;
-      if (nv[gi] > 0) {
-        load4(P.logits, P.logits_bf16, (int64_t)pos * P.ld, ig[gi], nv[gi], xg[gi]);
-        if (P.q) load4(P.q, P.q_bf16, qrow * P.ld_q, ig[gi], nv[gi], qg[gi]);
-        if (masked) mw[gi] = __ldg(P.bitmask + (size_t)pos * P.mask_words + (ig[gi] >> 5));
-      }
-    }
-#pragma unroll
-    for (int gi = 0; gi < kGroups; ++gi) {
-      if (nv[gi] <= 0) continue;
-      const int i0 = ig[gi];
-      float* x = xg[gi];
-      prelude_loaded(rc, i0, nv[gi], mw[gi], masked, aux, t0, brow, aux_on, x);
-      float rr[4];
-      bool any = false;
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        rr[k] = -1.0f;
-        if (x[k] > -INFINITY && k < nv[gi]) {
-          const float p = expf(x[k] - lse);
-          rr[k] = p - (P.q ? qg[gi][k] : (i0 + k == dtok ? 1.0f : 0.0f));
-          any |= rr[k] > 0.0f;
+      for (int gi = 0; gi < kGroups; ++gi) {
+        ig[gi] = s0 + 4 * tid + gi * 4 * kNT;
+        nv[gi] = min(4, t0 + nt - ig[gi]);
+        mw[gi] = 0xFFFFFFFFu;
+        if (nv[gi] > 0) {
+          load4(P.logits, P.logits_bf16, (int64_t)pos * P.ld, ig[gi], nv[gi], xg[gi]);
+          if (P.q) load4(P.q, P.q_bf16, qrow * P.ld_q, ig[gi], nv[gi], qg[gi]);
+          if (masked) mw[gi] = __ldg(P.bitmask + (size_t)pos * P.mask_words + (ig[gi] >> 5));
         }
       }
-      if (any) {
-        uint32_t c0 = (uint32_t)i0 >> 2, c1 = position, c2 = (uint32_t)r, c3 = 2u;
-        philox10(c0, c1, c2, c3, (uint32_t)seed, (uint32_t)(seed >> 32));
-        const uint32_t wd[4] = {c0, c1, c2, c3};
+#pragma unroll
+      for (int gi = 0; gi < kGroups; ++gi) {
+        if (nv[gi] <= 0) continue;
+        const int i0 = ig[gi];
+        float* x = xg[gi];
+        prelude_loaded(rc, i0, nv[gi], mw[gi], masked, aux, t0, brow, aux_on, x);
+        float rr[4];
+        bool any = false;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          if (rr[k] > 0.0f) {
-            const float g = gumbel_of(word_to_uniform(wd[(i0 + k) & 3]));
-            const unsigned long long sc = pack(f2key(__fadd_rn(logf(rr[k]), g)), (uint32_t)(i0 + k));
-            best = sc > best ? sc : best;
+          rr[k] = -1.0f;
+          if (x[k] > -INFINITY && k < nv[gi]) {
+            const float p = expf(x[k] - lse);
+            rr[k] = p - (P.q ? qg[gi][k] : (i0 + k == dtok ? 1.0f : 0.0f));
+            any |= rr[k] > 0.0f;
+          }
+        }
+        if (any) {
+          uint32_t c0 = (uint32_t)i0 >> 2, c1 = position, c2 = (uint32_t)r, c3 = 2u;
+          philox10(c0, c1, c2, c3, (uint32_t)seed, (uint32_t)(seed >> 32));
+          const uint32_t wd[4] = {c0, c1, c2, c3};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            if (rr[k] > 0.0f) {
+              const float g = gumbel_of(word_to_uniform(wd[(i0 + k) & 3]));
+              const unsigned long long sc = pack(f2key(__fadd_rn(logf(rr[k]), g)), (uint32_t)(i0 + k));
+              best = sc > best ? sc : best;
+            }
           }
         }
       }
