@@ -452,6 +452,21 @@ def test_config5_full():
     assert d.diag()[3] == 0
 
 
+def test_config4_one_hot_full():
+    # drafts without probabilities reject often: more queued residual entries
+    # than one round of 2048-token pieces covers, so the pass over the
+    # vocabulary takes longer pieces (streamed 2048 tokens at a time)
+    from spec_verification_gb300.runner import DeviceRun
+    w = W.with_one_hot_drafts(W.config4())
+    d = DeviceRun(w, candidates=True)
+    d()
+    rep = _oracle_chunks(w, d.results())
+    assert rep.ok(), rep
+    assert rep.ambiguous <= max(1, rep.checked // 200), rep
+    # more entries than the 608 pass CTAs cover in one round of 64 pieces each
+    assert d.diag()[2] > 608 // 64, d.diag()
+
+
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 def test_verify_low_noise_residual(dtype):
     """Untruncated stochastic rows whose target is the draft plus N(0, 0.02)
