@@ -238,9 +238,9 @@ __device__ __forceinline__ void stage2_position(const Params& P, int verify, int
     // order: a candidate's place is the number of candidates above it
     // (distinct values; empty slots (0) rank below every candidate).  What a
     // candidate needs that does not depend on its place is computed first,
-    // so that its latency overlaps the ordering: its fp64 softmax weight
+    // so that its latency overlaps the ordering: its softmax weight
     // w_t = exp(l_t - l_0) against the largest logit l_0 (each warp finds
-    // it), its Gumbel noise (one Philox draw: the sample of a sampled / bonus
+    // it; fp64 for a draft position, fp32 for a sample / bonus position), its Gumbel noise (one Philox draw: the sample of a sampled / bonus
     // position, or the truncated residual's of a draft) and, for a truncated
     // draft position, its q.  Weights are unused for point masses.
     const unsigned long long v = tid < kK ? sm.top[tid] : 0ull;
@@ -259,8 +259,11 @@ __device__ __forceinline__ void stage2_position(const Params& P, int verify, int
       const float lt = key2f(pk_key(v));
       const int32_t tk = pk_tok(v);
       if (rc.stoch && lt > -INFINITY && lz < INFINITY) {
-        wv = exp((double)lt - (double)lz);
-        if (!is_draft) wf = expf(__fsub_rn(lt, lz));
+        // fp64 for a draft position (its accept test and residual); a
+        // sample / bonus position takes fp32 and computes fp64 weights only
+        // in the rare fallback below (fp64 is the GPU's slowest pipe)
+        if (is_draft) wv = exp((double)lt - (double)lz);
+        else wf = expf(__fsub_rn(lt, lz));
       }
       if (rc.stoch && (!is_draft || rc.trunc))
         gv = gumbel_of(philox_uniform(seed, (uint32_t)tk, position, (uint32_t)r, is_draft ? 2u : 0u));
@@ -389,7 +392,8 @@ __device__ __forceinline__ void stage2_position(const Params& P, int verify, int
         }
         if (!f32) {
 #pragma unroll
-          for (int k = 0; k < 4; ++k) w[k] = sm.w[4 * lane + k];
+          for (int k = 0; k < 4; ++k)
+            w[k] = is_draft ? sm.w[4 * lane + k] : (fin[k] ? exp((double)l[k] - (double)l0) : 0.0);
           double ls = 0.0;
 #pragma unroll
           for (int k = 0; k < 4; ++k) ls += w[k];
