@@ -26,6 +26,13 @@ struct S3Smem {
   int pad;
 };
 
+// Word w (0..3) of a Philox block, by selects (an index into a local array
+// would go through local memory).  Groups start at multiples of 4 tokens, so
+// token i0 + k of a group takes word k of block i0 / 4.
+__device__ __forceinline__ uint32_t word_of4(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3, int w) {
+  return w == 0 ? c0 : (w == 1 ? c1 : (w == 2 ? c2 : c3));
+}
+
 // Processed logits of 4 consecutive tokens i0..i0+3 of one position (the
 // fp32 steps of the stage-1 prelude); counts come from the tile's aux table.
 __device__ __forceinline__ void prelude4(const Params& P, const RowCtx& rc, int pos, int i0, int n_valid,
@@ -212,11 +219,11 @@ __global__ void __launch_bounds__(kNT, 4) residual_kernel(const Params P) {
         if (any) {
           uint32_t c0 = (uint32_t)i0 >> 2, c1 = position, c2 = (uint32_t)r, c3 = 2u;
           philox10(c0, c1, c2, c3, (uint32_t)seed, (uint32_t)(seed >> 32));
-          const uint32_t wd[4] = {c0, c1, c2, c3};
+          
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             if (rr[k] > 0.0f) {
-              const float g = gumbel_of(word_to_uniform(wd[(i0 + k) & 3]));
+              const float g = gumbel_of(word_to_uniform(word_of4(c0, c1, c2, c3, k)));
               const unsigned long long sc = pack(f2key(__fadd_rn(logf(rr[k]), g)), (uint32_t)(i0 + k));
               best = sc > best ? sc : best;
             }
@@ -252,11 +259,11 @@ __global__ void __launch_bounds__(kNT, 4) residual_kernel(const Params P) {
             prelude4(P, rc, pos, i0, min(4, u0 + un - i0), aux, u0, brow, aux_on, x);
             uint32_t c0 = (uint32_t)i0 >> 2, c1 = position, c2 = (uint32_t)r, c3 = 2u;
             philox10(c0, c1, c2, c3, (uint32_t)seed, (uint32_t)(seed >> 32));
-            const uint32_t wd[4] = {c0, c1, c2, c3};
+            
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
               if (x[k] > -INFINITY && i0 + k < u0 + un) {
-                const float g = gumbel_of(word_to_uniform(wd[(i0 + k) & 3]));
+                const float g = gumbel_of(word_to_uniform(word_of4(c0, c1, c2, c3, k)));
                 const unsigned long long sc = pack(f2key(__fadd_rn(x[k], g)), (uint32_t)(i0 + k));
                 fb = sc > fb ? sc : fb;
               }
