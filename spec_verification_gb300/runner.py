@@ -152,16 +152,21 @@ class DeviceRun:
         for k, v in self.host.items():
             self.d[k].copy_(v, non_blocking=non_blocking)
 
-    def upload_split(self, main, copy_streams, events):
+    def upload_split(self, main, copy_streams, events, after=None):
         """Host -> device copy of every input with the streamed tensors
         (logits, draft probabilities) cut into row ranges, one per copy
         stream, so that several copies run at once; the small inputs go on
         `main`, which then waits for every copy stream.  events: one started
-        event plus one per copy stream (torch.cuda.Event, reused per call)."""
+        event plus one per copy stream (torch.cuda.Event, reused per call).
+        The copy streams start after `after` (an event: the last work that
+        read these device buffers) when given, else after everything queued
+        on `main` so far."""
         import torch
-        events[0].record(main)
+        if after is None:
+            events[0].record(main)
+            after = events[0]
         for st in copy_streams:
-            st.wait_event(events[0])
+            st.wait_event(after)
         for k, v in self.host.items():
             if k in ("logits", "draft_probs") and v.dim() == 2 and v.shape[0] >= len(copy_streams):
                 n = v.shape[0]
