@@ -374,8 +374,7 @@ ss_status launch(const ss_plan* pl, const ss::Params& P0, cudaStream_t st, bool 
   // least two stages per stage-1 CTA for the positions it can have.
   // Measured (us per call, fused against separate): 4 x 32000 fp32 18.8 /
   // 18.4 and a 64-row sampling call with lists 35.6 / 34.2 (not fused by
-  // default), 256 x 262144 fp32 73.3 / 74.8 and 32 rows x 5 positions of
-  // 131072 bf16 69.8 / 71.8 (fused by default).
+  // default), 256 x 262144 fp32 73.3 / 74.8 (fused by default).
   const bool shape_fuse = !aux && npos_bound * pl->Z >= 2LL * pl->grid1;
   const bool fused = allow_fusion && pl->exact == 0 && smem2 <= pl->fused_room &&
                      (pl->fuse == 1 || (pl->fuse == 0 && shape_fuse));
