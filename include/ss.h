@@ -7,7 +7,9 @@
  * sequence of kernel launches on the caller's stream whose launch shapes
  * depend only on the plan, so a call can be captured in a CUDA Graph and
  * replayed with new device-resident data (logits, parameters, draft offsets,
- * seeds).
+ * seeds).  Each call is also marked with NVTX ranges ("ss_sample" /
+ * "ss_verify", and one per launch: stage 1, stage 2, the residual pass) for
+ * profilers that record them.
  *
  * What is computed (page titles and sections of the source material):
  *  - "SonicSampler: unified tile-aware kernels for LLM sampling and

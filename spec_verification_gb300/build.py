@@ -66,7 +66,7 @@ def build(force: bool = False, verbose: bool = False, extra: list | None = None)
                     raise RuntimeError(f"nvcc failed for {cmd[-3]}")
     if jobs or not LIB.exists():
         tmp = LIB.with_suffix(f".{os.getpid()}.tmp.so")
-        cmd = [cc, *ARCH, "-shared", "-o", str(tmp), *map(str, objs), "-lcudart"]
+        cmd = [cc, *ARCH, "-shared", "-o", str(tmp), *map(str, objs), "-lcudart", "-ldl"]
         res = subprocess.run(cmd, capture_output=True, text=True)
         if res.returncode != 0:
             print(" ".join(cmd), res.stdout, res.stderr)

@@ -1,6 +1,7 @@
 // Host side of libss.so: plans, argument checks, workspace layout and the
 // fixed launch sequence of ss_sample / ss_verify (see include/ss.h).
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <algorithm>
 #include <cstdio>
@@ -342,8 +343,16 @@ int seg_cap_for(const ss_plan* pl, int B) {
   return cap;
 }
 
+// NVTX ranges (a call, and each launch in it) for profilers that record
+// them; without a tool attached each push or pop is a test of a pointer.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+};
+
 ss_status launch(const ss_plan* pl, const ss::Params& P0, cudaStream_t st, bool verify, void* const* ev,
                  bool allow_fusion = true) {
+  const NvtxRange call_range(verify ? "ss_verify" : "ss_sample");
   ss::Params P = P0;
   P.seg_cap = seg_cap_for(pl, P.B);
   P.exact_on = pl->exact;
@@ -394,6 +403,7 @@ ss_status launch(const ss_plan* pl, const ss::Params& P0, cudaStream_t st, bool 
   const bool lean_only = aux && !verify && pl->exact == 0 && !fused && listed_max <= ss::stage1_hash_tokens();
   const bool dual = aux && !lean_only && pl->exact == 0 && !fused && npos_bound * pl->Z >= 10LL * pl->grid1;
   P.dispatch = 0;
+  nvtxRangePushA(fused ? "ss stage 1 + 2" : "ss stage 1");
   if (lean_only) {
     ss::stage1_launch_lean(pl->ldt == SS_BF16, pl->grid1, pl->smem1, st, P);
   } else {
@@ -405,10 +415,17 @@ ss_status launch(const ss_plan* pl, const ss::Params& P0, cudaStream_t st, bool 
     ss::stage1_launch(pl->ldt == SS_BF16, pl->exact != 0, aux, P.cu_draft != nullptr, fused, pl->grid1, pl->smem1, st,
                       P);
   }
+  nvtxRangePop();
   rec(1);
-  if (!fused) ss::stage2_kernel<<<grid2, ss::stage2_threads(), smem2, st>>>(P, verify ? 1 : 0);
+  if (!fused) {
+    const NvtxRange r2("ss stage 2");
+    ss::stage2_kernel<<<grid2, ss::stage2_threads(), smem2, st>>>(P, verify ? 1 : 0);
+  }
   rec(2);
-  if (verify) ss::residual_kernel<<<pl->grid3, ss::kNT, pl->smem3, st>>>(P);
+  if (verify) {
+    const NvtxRange r3("ss residual pass");
+    ss::residual_kernel<<<pl->grid3, ss::kNT, pl->smem3, st>>>(P);
+  }
   rec(3);
   pl->last_launches = 1 + (dual ? 1 : 0) + (fused ? 0 : 1) + (verify ? 1 : 0);
   if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
