@@ -3,8 +3,10 @@
 // top-128, every logit streamed from HBM once.
 //
 // Work split.  Each target position's row is cut into Z_v stages of B_N
-// tokens; the npos * Z_v stages, position-major, are divided into
-// G = min(grid, npos * Z_v) nearly equal contiguous ranges, one per CTA.  The
+// tokens; the npos * Z_v stages, position-major, are divided into contiguous
+// ranges, one per CTA: G = min(grid, npos * Z_v) nearly equal ranges, or,
+// when the grid holds two or more CTAs per position, ranges that split each
+// position evenly and never cross a position boundary.  The
 // part of a CTA's range inside one row is a segment, so a row has 1..Z_v
 // segments; each segment leaves its exact top-128 (packed key << 32 | ~token)
 // in the staging buffer and stage 2 merges a row's segments (seg_start /
@@ -32,9 +34,10 @@
 //    top-128;
 //  - history / draft / bias tokens need their count and bias entries, so they
 //    are kept out of that path: per segment they are listed in a hash table
-//    (which the rare appends consult, when the appending thread's filter of
-//    its listed elements does not rule them out) and their exact values, read straight
-//    from HBM, are the segment's first candidates; very long histories (and
+//    (which a rare append consults when the appending thread's 32-bit filter
+//    of the listed tokens among its elements does not rule its token out)
+//    and their exact values, read straight from HBM, are the segment's first
+//    candidates; very long histories (and
 //    verify positions that need the full-vocabulary normaliser) use a
 //    per-stage count table instead, appending those tokens as their stage
 //    streams through;
