@@ -211,20 +211,23 @@ __global__ void __launch_bounds__(kNT, 4) residual_kernel(const Params P) {
         for (int k = 0; k < 4; ++k) {
           rr[k] = -1.0f;
           if (x[k] > -INFINITY && k < nv[gi]) {
-            const float p = expf(x[k] - lse);
-            rr[k] = p - (P.q ? qg[gi][k] : (i0 + k == dtok ? 1.0f : 0.0f));
+            // q one-hot on the draft (drafts without probabilities): r_i = p_i
+            // for every other token and 0 at the draft, so ln r_i is l_i - LSE
+            // with no exp or log; rr only marks the support then
+            if (P.q) rr[k] = expf(x[k] - lse) - qg[gi][k];
+            else rr[k] = i0 + k == dtok ? 0.0f : 1.0f;
             any |= rr[k] > 0.0f;
           }
         }
         if (any) {
           uint32_t c0 = (uint32_t)i0 >> 2, c1 = position, c2 = (uint32_t)r, c3 = 2u;
           philox10(c0, c1, c2, c3, (uint32_t)seed, (uint32_t)(seed >> 32));
-          
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             if (rr[k] > 0.0f) {
               const float g = gumbel_of(word_to_uniform(word_of4(c0, c1, c2, c3, k)));
-              const unsigned long long sc = pack(f2key(__fadd_rn(logf(rr[k]), g)), (uint32_t)(i0 + k));
+              const float lr = P.q ? logf(rr[k]) : __fsub_rn(x[k], lse);
+              const unsigned long long sc = pack(f2key(__fadd_rn(lr, g)), (uint32_t)(i0 + k));
               best = sc > best ? sc : best;
             }
           }
